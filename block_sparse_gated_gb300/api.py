@@ -1,0 +1,221 @@
+"""torch-facing wrappers over the C ABI: argument marshalling only.
+
+Every step of the computation runs in libbsfa.so's CUDA kernels; torch
+provides device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _native
+
+GATE_THRESHOLD, GATE_LAMBDA, GATE_NONE = 0, 1, 2
+_MODES = {"threshold": GATE_THRESHOLD, "lambda": GATE_LAMBDA, "none": GATE_NONE,
+          "dense": GATE_NONE}
+
+
+class BsfaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        msg = _native.lib().bsfa_status_string(status).decode()
+        super().__init__(f"bsfa status {status} ({msg}){': ' + what if what else ''}")
+        self.status = status
+
+
+def _check(status: int, what: str = ""):
+    if status != 0:
+        raise BsfaError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _strides_bhtd(t: torch.Tensor, layout: str, varlen: bool):
+    """Element strides {batch, head, token} of a bf16 tensor with d contiguous."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError("expected a bfloat16 tensor")
+    if t.stride(-1) != 1:
+        raise ValueError("the head dimension must be contiguous")
+    s = t.stride()
+    if varlen:
+        if t.dim() != 3:
+            raise ValueError("varlen tensors are 3-D")
+        if layout == "htd":
+            return (0, s[0], s[1]), t.shape[0], t.shape[1]
+        if layout == "thd":
+            return (0, s[1], s[0]), t.shape[1], t.shape[0]
+        raise ValueError(layout)
+    if t.dim() == 3:  # [H, L, d] single sequence
+        return (t.shape[0] * s[0], s[0], s[1]), t.shape[0], t.shape[1]
+    if t.dim() != 4:
+        raise ValueError("batched tensors are 4-D")
+    if layout == "bhld":
+        return (s[0], s[1], s[2]), t.shape[1], t.shape[2]
+    if layout == "blhd":
+        return (s[0], s[2], s[1]), t.shape[2], t.shape[1]
+    raise ValueError(layout)
+
+
+def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, softmax_scale,
+            mode, thresholds, log_lambda):
+    varlen = cu_seqlens is not None
+    if layout is None:
+        layout = "htd" if varlen else "bhld"
+    qs, Hq, Lq = _strides_bhtd(q, layout, varlen)
+    ks, Hkv, Lk = _strides_bhtd(k, layout, varlen)
+    vs, Hv, Lv = _strides_bhtd(v, layout, varlen)
+    os_, Ho, Lo = _strides_bhtd(o, layout, varlen)
+    if not (Lq == Lk == Lv == Lo) or Hv != Hkv or Ho != Hq:
+        raise ValueError("Q/K/V/O shapes disagree")
+    d = q.shape[-1]
+    p = _native.FwdParams()
+    p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+    p.q_stride[:], p.k_stride[:], p.v_stride[:], p.o_stride[:] = qs, ks, vs, os_
+    if varlen:
+        p.batch = cu_seqlens.numel() - 1
+        p.cu_seqlens = cu_seqlens.data_ptr()
+        p.max_seqlen = int(max_seqlen)
+    else:
+        p.batch = 1 if q.dim() == 3 else q.shape[0]
+        p.cu_seqlens = None
+        p.max_seqlen = 0
+    p.num_heads_q, p.num_heads_kv, p.seqlen, p.head_dim = Hq, Hkv, Lq, d
+    p.block_q, p.block_k = block_q, block_k
+    p.softmax_scale = float(softmax_scale) if softmax_scale else 0.0
+    p.mode = _MODES[mode] if isinstance(mode, str) else int(mode)
+    if thresholds is not None:
+        if thresholds.dtype != torch.float32 or thresholds.dim() != 2 or not thresholds.is_contiguous():
+            raise ValueError("thresholds must be a contiguous float32 [Hq, nT] tensor")
+        p.thresholds, p.thresholds_nq = thresholds.data_ptr(), thresholds.shape[1]
+    else:
+        p.thresholds, p.thresholds_nq = None, 0
+    p.log_lambda = float(log_lambda) if log_lambda is not None else 0.0
+    return p
+
+
+def bitmap_shape(num_heads_q: int, *, block_q: int, block_k: int, seqlens) -> tuple[int, int, int]:
+    """(rows, Hq, words) of the kept-block bitmap for sequences of lengths
+    ``seqlens``: rows = sum ceil(L_b/Bq), words = ceil(ceil(max L_b/Bk)/32)."""
+    rows = sum((int(L) + block_q - 1) // block_q for L in seqlens)
+    mx = max((int(L) for L in seqlens), default=0)
+    words = ((mx + block_k - 1) // block_k + 31) // 32
+    return rows, num_heads_q, words
+
+
+def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="threshold",
+            thresholds=None, log_lambda=None, cu_seqlens=None, max_seqlen=None, layout=None,
+            out=None, return_bitmap=False, return_lse=False, return_counts=False,
+            workspace=None, stream=None):
+    """Gated causal prefill.  Batched: q [B, Hq, L, d] (layout "bhld") or
+    [B, L, Hq, d] ("blhd"); varlen (cu_seqlens int32 on the device): q [Hq, T, d]
+    ("htd") or [T, Hq, d] ("thd").  Returns a dict with "out" and, on request,
+    "bitmap" (int32 [rows, Hq, words], bit j of word j//32 = keep), "lse"
+    (float32 [Hq, rows_of_tokens]) and "counts" (int64 [3]: kept candidates,
+    candidates, diagonal-region blocks)."""
+    if out is None:
+        out = torch.empty_like(q)
+    p = _params(q, k, v, out, layout=layout, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
+                block_q=block_q, block_k=block_k, softmax_scale=softmax_scale, mode=mode,
+                thresholds=thresholds, log_lambda=log_lambda)
+    L = _native.lib()
+    res = {"out": out}
+    dev = q.device
+    if return_bitmap:
+        if cu_seqlens is not None:
+            cu = cu_seqlens.cpu().tolist()
+            lens = [b - a for a, b in zip(cu[:-1], cu[1:])]
+        else:
+            lens = [p.seqlen] * p.batch
+        rows, H, _ = bitmap_shape(p.num_heads_q, block_q=block_q, block_k=block_k, seqlens=lens)
+        w = ctypes.c_int(0)
+        _check(L.bsfa_bitmap_words_per_row(ctypes.byref(p), ctypes.byref(w)), "bitmap words")
+        words = w.value  # the kernel's row pitch (from max_seqlen in varlen mode)
+        bm = torch.empty((max(rows, 1), H, max(words, 1)), dtype=torch.int32, device=dev)
+        p.kept_bitmap = bm.data_ptr()
+        res["bitmap"] = bm[:rows]
+    if return_lse:
+        rows_tok = p.seqlen if cu_seqlens is not None else p.batch * p.seqlen
+        lse = torch.empty((p.num_heads_q, rows_tok), dtype=torch.float32, device=dev)
+        p.lse = lse.data_ptr()
+        res["lse"] = lse
+    if return_counts:
+        cnt = torch.empty(3, dtype=torch.int64, device=dev)
+        p.block_counts = cnt.data_ptr()
+        res["counts"] = cnt
+    need = L.bsfa_prefill_workspace_size(ctypes.byref(p))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    _check(L.bsfa_prefill_fwd(ctypes.byref(p), _stream(stream)), "bsfa_prefill_fwd")
+    return res
+
+
+def prefill_workspace_bytes(q, k, v, **kw) -> int:
+    """Workspace bytes bsfa_prefill_fwd needs for this call's shapes."""
+    out = kw.pop("out", None)
+    p = _params(q, k, v, out if out is not None else q, layout=kw.get("layout"),
+                cu_seqlens=kw.get("cu_seqlens"), max_seqlen=kw.get("max_seqlen"),
+                block_q=kw.get("block_q", 128), block_k=kw.get("block_k", 128),
+                softmax_scale=kw.get("softmax_scale"), mode=kw.get("mode", "threshold"),
+                thresholds=kw.get("thresholds"), log_lambda=kw.get("log_lambda"))
+    return int(_native.lib().bsfa_prefill_workspace_size(ctypes.byref(p)))
+
+
+def calibrate(q_samples, k_samples, ks, *, block_q=128, block_k=128, softmax_scale=None,
+              out=None, workspace=None, stream=None):
+    """Thresholds [len(ks), Hq, ceil(L/Bq)] (float32, device) from equal-length
+    samples q [Hq, L, d] / k [Hkv, L, d] (bf16, d contiguous)."""
+    n = len(q_samples)
+    if n == 0 or n != len(k_samples):
+        raise ValueError("need matching non-empty sample lists")
+    q0, k0 = q_samples[0], k_samples[0]
+    Hq, Ltok, d = q0.shape
+    Hkv = k0.shape[0]
+    for t in list(q_samples) + list(k_samples):
+        if t.dtype != torch.bfloat16 or t.stride(-1) != 1 or t.shape[1] != Ltok or t.shape[2] != d:
+            raise ValueError("samples must be bf16 [H, L, d] with d contiguous and equal L")
+    nq = (Ltok + block_q - 1) // block_q
+    if out is None:
+        out = torch.empty((len(ks), Hq, nq), dtype=torch.float32, device=q0.device)
+    L = _native.lib()
+    need = L.bsfa_calibrate_workspace_size(Hq, Ltok, block_q, block_k)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q0.device)
+    qp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in q_samples])
+    kp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in k_samples])
+    qst = (ctypes.c_int64 * 2)(q0.stride(0), q0.stride(1))
+    kst = (ctypes.c_int64 * 2)(k0.stride(0), k0.stride(1))
+    for t in q_samples[1:]:
+        if t.stride()[:2] != q0.stride()[:2]:
+            raise ValueError("all q samples must share strides")
+    for t in k_samples[1:]:
+        if t.stride()[:2] != k0.stride()[:2]:
+            raise ValueError("all k samples must share strides")
+    karr = (ctypes.c_int * len(ks))(*[int(x) for x in ks])
+    scale = float(softmax_scale) if softmax_scale else 0.0
+    _check(L.bsfa_calibrate(qp, kp, n, Hq, Hkv, Ltok, d, qst, kst, block_q, block_k, scale,
+                            karr, len(ks), ctypes.c_void_p(out.data_ptr()),
+                            ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                            _stream(stream)), "bsfa_calibrate")
+    return out
+
+
+def device_error(stream=None) -> int:
+    """Synchronise and return (and clear) the device error word; 0 if clean."""
+    code = ctypes.c_uint(0)
+    st = _native.lib().bsfa_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (0, 4):
+        _check(st, "bsfa_device_error")
+    return int(code.value)
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

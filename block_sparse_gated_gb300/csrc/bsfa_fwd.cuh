@@ -1,0 +1,715 @@
+// bsfa_fwd.cuh -- the persistent, warp-specialised gated prefill kernel for
+// sm_103a, and its calibration variant.
+//
+// What it computes ("Block Sparse Flash Attention", Key Designs 2 and 3; the
+// lambda gate from "Skipping attention blocks was the easy part", section
+// "Vote, then skip"): for every causally visible 128x128 score tile
+// S = Q K^T (tcgen05 MMA, bf16 in, fp32 in TMEM) the semantic Bq x Bk blocks
+// inside it are gated; a kept block goes through online softmax and O += P V
+// (P in TMEM, V by TMA only after the decision); a skipped block leaves the
+// running max, the normaliser and O untouched and its V is never fetched.
+//
+// Roles (one CTA per SM, persistent over a heaviest-first unit list):
+//   warp 0          TMA producer: Q per unit, K for every visible tile, V for
+//                   tiles that some slot keeps (issued after the decision).
+//   warp 1          MMA issuer (one thread): S_s = Q_s K^T, O_s += P_s V.
+//                   Also owns the TMEM allocation.
+//   warps 4..       one softmax warpgroup per query slot s (NQ slots = NQ
+//                   query heads of one GQA group sharing the K/V stream);
+//                   thread t owns query row t of the slot's 128-row tile.
+//
+// TMEM columns: S_s at [128 s, 128 s + 128) (P_s overwrites its first 64
+// columns as packed bf16 pairs), O_s at [128 NQ + D s, 128 NQ + D (s+1)).
+#pragma once
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "ptx.cuh"
+
+namespace bsfa {
+
+constexpr int TILE = 128;
+constexpr int KST = 2;  // K ring stages
+constexpr int VST = 2;  // V ring stages
+constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
+constexpr float RESCALE_LOG2 = 8.0f;  // lazy rescale: P may grow to 2^8 before O is rescaled
+
+// Device error word codes (site of the wait that ran out).
+enum : unsigned {
+  ERR_WAIT_Q_EMPTY = 0x101, ERR_WAIT_K_EMPTY, ERR_WAIT_V_EMPTY, ERR_WAIT_DEC,
+  ERR_WAIT_Q_FULL, ERR_WAIT_K_FULL, ERR_WAIT_V_FULL, ERR_WAIT_P_FULL, ERR_WAIT_O_EMPTY,
+  ERR_WAIT_S_FULL, ERR_WAIT_WG, ERR_WAIT_O_FULL, ERR_WAIT_DRAIN
+};
+
+struct DevParams {
+  __nv_bfloat16* o;
+  long long o_sb, o_sh, o_st;
+  int Hq, Hkv, group, pairs;  // pairs = group / NQ
+  int varlen;
+  int batch_len;              // batched layout: tokens per sequence (lse row = b*batch_len + pos)
+  int Bq, Bk;
+  float sigma, sigma_log2;
+  int mode;                   // 0 threshold, 1 lambda, 2 dense
+  const float* thr;
+  int nT;
+  float log_lambda;
+  uint32_t* bitmap;
+  int words;                  // bitmap words per row; layout [query-block rows][Hq][words]
+  float* lse;
+  long long lse_rows;
+  unsigned long long* counts; // [3]
+  const int4* seqinfo;        // {tok0, len, rowbase, bcoord}
+  const int2* tiles;          // {b, I} sorted by I descending
+  const int* ntiles_total;
+  float* blockmax;            // calibration: [Hq][cal_nq][cal_nk]
+  int cal_nq, cal_nk;
+  unsigned* err;
+};
+
+template <int D, int NQ>
+struct Ctrl {
+  uint64_t q_full[NQ];
+  uint64_t q_empty;
+  uint64_t k_full[KST], k_empty[KST];
+  uint64_t v_full[VST], v_empty[VST];
+  uint64_t s_full[NQ], p_full[NQ], o_full[NQ], o_empty[NQ];
+  uint64_t dec_full[NQ][2];
+  uint64_t wg[NQ][2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t dec[NQ][2];
+  float red[NQ][2][4][2];
+  int abort;
+};
+
+template <int D, int NQ, bool CALIB>
+struct Layout {
+  static constexpr int TB = TILE * D * 2;  // bytes of one 128-row bf16 tile
+  static constexpr int NV = CALIB ? 0 : VST;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + NQ * TB;
+  static constexpr int V_OFF = K_OFF + KST * TB;
+  static constexpr int C_OFF = V_OFF + NV * TB;
+  // + alignment slack; at least 120 KB so that a single CTA is resident per SM
+  // (the persistent grid assumes it and the TMEM allocation is not shared).
+  static constexpr int RAW = C_OFF + (int)sizeof(Ctrl<D, NQ>) + 1024;
+  static constexpr int BYTES = RAW > 120 * 1024 ? RAW : 120 * 1024;
+  static constexpr int NCOLS = (NQ * 128 + NQ * D) <= 256 ? 256 : 512;
+  static constexpr int NTHREADS = 128 + 128 * NQ;
+};
+
+// Bounded wait: true when the phase of `parity` completed; false after the
+// time bound (error word set, abort raised) or when another role aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         unsigned* err, unsigned site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 31u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > WAIT_TIMEOUT_NS) {
+        *abort = 1;
+        atomicCAS(err, 0u, site);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait used only on the abort path: ignores the abort flag so that
+// copies / MMAs already in flight can land before the CTA releases resources.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > WAIT_TIMEOUT_NS / 20) return;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Semantic block class of key block j for query block i (length-L sequence):
+// 1 = candidate (every key precedes every row), 2 = diagonal region, 0 = none.
+__device__ __forceinline__ int block_class(int i, int j, int Bq, int Bk, int L) {
+  const int first_row = i * Bq;
+  const int last_row = min((i + 1) * Bq, L) - 1;
+  const int first_key = j * Bk;
+  if (first_row > last_row || first_key >= L) return 0;
+  if ((j + 1) * Bk <= first_row) return 1;
+  if (first_key <= last_row) return 2;
+  return 0;
+}
+
+template <int D, int NQ, bool GATING, bool CALIB>
+__global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
+    bsfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const DevParams p) {
+  using LY = Layout<D, NQ, CALIB>;
+  constexpr int TB = LY::TB;
+  constexpr int HALF = TILE * 128;  // bytes of one 64-column swizzled half
+  constexpr int NHALF = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = base + LY::Q_OFF;
+  uint8_t* sK = base + LY::K_OFF;
+  uint8_t* sV = base + LY::V_OFF;
+  Ctrl<D, NQ>* c = reinterpret_cast<Ctrl<D, NQ>*>(base + LY::C_OFF);
+  volatile int* abort = &c->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(&c->q_full[s], 1);
+      mbar_init(&c->s_full[s], 1);
+      mbar_init(&c->p_full[s], 128);
+      mbar_init(&c->o_full[s], 1);
+      mbar_init(&c->o_empty[s], 128);
+      mbar_init(&c->dec_full[s][0], 1);
+      mbar_init(&c->dec_full[s][1], 1);
+      mbar_init(&c->wg[s][0], 4);
+      mbar_init(&c->wg[s][1], 4);
+    }
+    mbar_init(&c->q_empty, 1);
+    for (int i = 0; i < KST; ++i) {
+      mbar_init(&c->k_full[i], 1);
+      mbar_init(&c->k_empty[i], 1);
+    }
+    for (int i = 0; i < VST; ++i) {
+      mbar_init(&c->v_full[i], 1);
+      mbar_init(&c->v_empty[i], 1);
+    }
+    mbar_init(&c->drain, 1);
+    c->abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    if (!CALIB) prefetch_tensormap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(&c->tmem_base, LY::NCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c->tmem_base;
+
+  const int HP = p.Hkv * p.pairs;
+  const int total_units = (*p.ntiles_total) * HP;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
+      int last_q = -1;  // index of the last unit whose Q load was issued
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+        const int2 t = p.tiles[u / HP];
+        const int hp = u % HP, kvh = hp / p.pairs, pr = hp % p.pairs;
+        const int4 si = p.seqinfo[t.x];
+        const int I = t.y, nkt = I + 1;
+        const int row0 = si.x + I * TILE;
+        if (!(ok = wait_bar(&c->q_empty, (uc & 1) ^ 1, abort, p.err, ERR_WAIT_Q_EMPTY))) break;
+        for (int s = 0; s < NQ; ++s) {
+          const int h = kvh * p.group + pr * NQ + s;
+          mbar_arrive_expect_tx(&c->q_full[s], TB);
+          for (int hf = 0; hf < NHALF; ++hf)
+            tma_load_4d(sQ + s * TB + hf * HALF, &tmQ, &c->q_full[s], hf * 64, row0, h, si.w);
+        }
+        last_q = static_cast<int>(uc);
+        auto issue_k = [&](int J) -> bool {
+          const uint32_t st = kc % KST;
+          if (!wait_bar(&c->k_empty[st], ((kc / KST) & 1) ^ 1, abort, p.err, ERR_WAIT_K_EMPTY))
+            return false;
+          mbar_arrive_expect_tx(&c->k_full[st], TB);
+          for (int hf = 0; hf < NHALF; ++hf)
+            tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64,
+                        si.x + J * TILE, kvh, si.w);
+          ++kc;
+          return true;
+        };
+        if (!(ok = issue_k(0))) break;
+        for (int J = 0; J < nkt; ++J, ++tc) {
+          if (J + 1 < nkt && !(ok = issue_k(J + 1))) break;
+          if constexpr (!CALIB) {
+            bool need = true;
+            if constexpr (GATING) {
+              need = false;
+              for (int s = 0; s < NQ; ++s) {
+                if (!(ok = wait_bar(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
+                                    ERR_WAIT_DEC)))
+                  break;
+                if (c->dec[s][tc & 1] != 0u) {
+                  need = true;
+                  break;
+                }
+              }
+              if (!ok) break;
+            }
+            if (need) {
+              const uint32_t st = vc % VST;
+              if (!(ok = wait_bar(&c->v_empty[st], ((vc / VST) & 1) ^ 1, abort, p.err,
+                                  ERR_WAIT_V_EMPTY)))
+                break;
+              mbar_arrive_expect_tx(&c->v_full[st], TB);
+              for (int hf = 0; hf < NHALF; ++hf)
+                tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64,
+                            si.x + J * TILE, kvh, si.w);
+              ++vc;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Let every copy already issued land before the CTA can exit.
+        for (int s = 0; s < NQ && last_q >= 0; ++s) drain_wait(&c->q_full[s], last_q & 1);
+        for (uint32_t i = 0; i < KST && i < kc; ++i) {
+          const uint32_t f = kc - 1 - i;
+          drain_wait(&c->k_full[f % KST], (f / KST) & 1);
+        }
+        for (uint32_t i = 0; i < VST && i < vc; ++i) {
+          const uint32_t f = vc - 1 - i;
+          drain_wait(&c->v_full[f % VST], (f / VST) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
+      uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
+      bool ok = true;
+      auto issue_qk = [&](int s, uint32_t st) {
+        const uint32_t d_tmem = tmem + s * 128;
+        const uint32_t qa = smem_u32(sQ + s * TB), ka = smem_u32(sK + st * TB);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+          umma_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                  IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int s, uint32_t st, uint32_t acc) {
+        const uint32_t d_tmem = tmem + NQ * 128 + s * D;
+        const uint32_t va = smem_u32(sV + st * TB);
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          umma_ts(d_tmem, tmem + s * 128 + kk * 8, smem_desc_sw128(va + kk * 2048, HALF, 1024),
+                  IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
+      };
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+        const int2 t = p.tiles[u / HP];
+        const int nkt = t.y + 1;
+        for (int s = 0; s < NQ && ok; ++s)
+          ok = wait_bar(&c->q_full[s], uc & 1, abort, p.err, ERR_WAIT_Q_FULL);
+        if (!ok) break;
+        {
+          const uint32_t st = kc % KST;
+          if (!(ok = wait_bar(&c->k_full[st], (kc / KST) & 1, abort, p.err, ERR_WAIT_K_FULL))) break;
+          tc_fence_after();
+          for (int s = 0; s < NQ; ++s) {
+            issue_qk(s, st);
+            umma_commit(&c->s_full[s]);
+          }
+          umma_commit(&c->k_empty[st]);
+          ++kc;
+          if (nkt == 1) umma_commit(&c->q_empty);
+        }
+        bool first[NQ];
+        for (int s = 0; s < NQ; ++s) first[s] = true;
+        for (int J = 0; J < nkt && ok; ++J, ++tc) {
+          const int tb = tc & 1;
+          const uint32_t vst = vc % VST;
+          const uint32_t kst = kc % KST;
+          bool vready = false, any = false;
+          for (int s = 0; s < NQ; ++s) {
+            if (!(ok = wait_bar(&c->p_full[s], tc & 1, abort, p.err, ERR_WAIT_P_FULL))) break;
+            tc_fence_after();
+            if constexpr (!CALIB) {
+              const uint32_t dec = GATING ? c->dec[s][tb] : 1u;
+              if (dec != 0u) {
+                any = true;
+                if (!vready) {
+                  if (!(ok = wait_bar(&c->v_full[vst], (vc / VST) & 1, abort, p.err,
+                                      ERR_WAIT_V_FULL)))
+                    break;
+                  tc_fence_after();
+                  vready = true;
+                }
+                uint32_t acc = 1u;
+                if (first[s]) {
+                  if (!(ok = wait_bar(&c->o_empty[s], (uc & 1) ^ 1, abort, p.err,
+                                      ERR_WAIT_O_EMPTY)))
+                    break;
+                  tc_fence_after();
+                  acc = 0u;
+                  first[s] = false;
+                }
+                issue_pv(s, vst, acc);
+              }
+            }
+            if (J + 1 < nkt) {
+              if (s == 0) {
+                if (!(ok = wait_bar(&c->k_full[kst], (kc / KST) & 1, abort, p.err,
+                                    ERR_WAIT_K_FULL)))
+                  break;
+                tc_fence_after();
+              }
+              issue_qk(s, kst);
+              umma_commit(&c->s_full[s]);
+              if (s == NQ - 1) {
+                umma_commit(&c->k_empty[kst]);
+                ++kc;
+                if (J + 1 == nkt - 1) umma_commit(&c->q_empty);
+              }
+            }
+          }
+          if (!ok) break;
+          if (!CALIB && any) {
+            umma_commit(&c->v_empty[vst]);
+            ++vc;
+          }
+        }
+        if (!ok) break;
+        if constexpr (!CALIB)
+          for (int s = 0; s < NQ; ++s) umma_commit(&c->o_full[s]);
+      }
+      // Drain: every issued MMA completes before TMEM can be released.
+      umma_commit(&c->drain);
+      drain_wait(&c->drain, 0);
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax
+    const int s = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t tlane = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + tlane + s * 128;
+    const uint32_t tO = tmem + tlane + NQ * 128 + s * D;
+    const int QS = TILE / p.Bq, KS = TILE / p.Bk;
+    const int myqs = (p.Bq == 64) ? (row >> 6) : 0;
+    const bool leader = (row % p.Bq) == 0;  // first row of its semantic query block
+    uint32_t tc = 0, uc = 0, nsync = 0;
+    bool ok = true;
+    unsigned long long cnt_kept = 0, cnt_cand = 0, cnt_diag = 0;
+
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+      const int2 t = p.tiles[u / HP];
+      const int hp = u % HP, kvh = hp / p.pairs, pr = hp % p.pairs;
+      const int4 si = p.seqinfo[t.x];
+      const int I = t.y, nkt = I + 1, len = si.y;
+      const int h = kvh * p.group + pr * NQ + s;
+      const int qpos = I * TILE + row;
+      const bool rvalid = qpos < len;
+      const int iq_base = (I * TILE) / p.Bq;  // semantic query block of row 0
+      const int my_i = iq_base + myqs;
+      float thr[2] = {0.f, 0.f};
+      if (GATING && !CALIB && p.mode == 0) {
+        for (int q = 0; q < QS; ++q)
+          thr[q] = p.thr[(long long)h * p.nT + min(iq_base + q, p.nT - 1)];
+      }
+      float m_used = -CUDART_INF_F, m_true = -CUDART_INF_F, l = 0.f;
+      bool o_init = false;
+      uint32_t bm_word = 0;
+      int bm_idx = 0;
+      const bool bm_on = (p.bitmap != nullptr) && leader && (my_i * p.Bq < len);
+      const long long bm_row = ((long long)(si.z + my_i) * p.Hq + h) * (long long)p.words;
+
+      for (int J = 0; J < nkt; ++J, ++tc) {
+        const int tb = tc & 1;
+        if (!(ok = wait_bar(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL))) break;
+        tc_fence_after();
+        // Pass 1: row maxima of the two 64-key halves (the causal mask only
+        // reaches into the last tile, J == I, where key column c > row is
+        // invisible).  S stays in TMEM; pass 2 reads it again.
+        const bool diag_tile = (J == I);
+        float rm0 = -CUDART_INF_F, rm1 = -CUDART_INF_F;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sr[2][32];
+          tmem_ld32(tS + hf * 64, sr[0]);
+          tmem_ld32(tS + hf * 64 + 32, sr[1]);
+          tmem_wait_ld();
+          float mx = -CUDART_INF_F;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const float x = __uint_as_float(sr[e >> 5][e & 31]);
+            mx = (diag_tile && (hf * 64 + e) > row) ? mx : fmaxf(mx, x);
+          }
+          if (hf == 0) rm0 = mx; else rm1 = mx;
+        }
+        if (KS == 1) {
+          rm0 = fmaxf(rm0, rm1);
+          rm1 = rm0;
+        }
+
+        // Block classes of the (query, key) sub-blocks of this tile.
+        int cls[2][2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            cls[q][k] = (q < QS && k < KS)
+                            ? block_class(iq_base + q, (J * TILE) / p.Bk + k, p.Bq, p.Bk, len)
+                            : 0;
+
+        if constexpr (CALIB) {
+          // Calibration: record sigma * s_max for candidate blocks.
+          const float v0 = rvalid ? rm0 : -CUDART_INF_F;
+          const float v1 = rvalid ? rm1 : -CUDART_INF_F;
+          const float w0 = warp_max(v0), w1 = warp_max(v1);
+          const int rb = nsync & 1;
+          if (lane == 0) {
+            c->red[s][rb][wq][0] = w0;
+            c->red[s][rb][wq][1] = w1;
+            mbar_arrive(&c->wg[s][rb]);
+          }
+          if (!(ok = wait_bar(&c->wg[s][rb], (nsync >> 1) & 1, abort, p.err, ERR_WAIT_WG)))
+            break;
+          ++nsync;
+          if (row == 0) {
+            for (int q = 0; q < QS; ++q)
+              for (int k = 0; k < KS; ++k) {
+                if (cls[q][k] != 1) continue;
+                float mx = -CUDART_INF_F;
+                for (int w = 0; w < 4; ++w)
+                  if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][rb][w][k]);
+                const long long idx =
+                    ((long long)h * p.cal_nq + iq_base + q) * p.cal_nk + (J * TILE) / p.Bk + k;
+                p.blockmax[idx] = mx * p.sigma;
+              }
+          }
+          tc_fence_before();
+          mbar_arrive(&c->p_full[s]);
+          continue;
+        } else {
+          // ---- gate: decide every sub-block of this tile
+          bool keep[2][2];
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int k = 0; k < 2; ++k) keep[q][k] = cls[q][k] != 0;
+          if constexpr (GATING) {
+            if (p.mode == 0) {
+              const float v0 = rvalid ? rm0 : -CUDART_INF_F;
+              const float v1 = rvalid ? rm1 : -CUDART_INF_F;
+              const float w0 = warp_max(v0), w1 = warp_max(v1);
+              const int rb = nsync & 1;
+              if (lane == 0) {
+                c->red[s][rb][wq][0] = w0;
+                c->red[s][rb][wq][1] = w1;
+                mbar_arrive(&c->wg[s][rb]);
+              }
+              if (!(ok = wait_bar(&c->wg[s][rb], (nsync >> 1) & 1, abort, p.err, ERR_WAIT_WG)))
+                break;
+              ++nsync;
+#pragma unroll
+              for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  if (cls[q][k] != 1) continue;
+                  float mx = -CUDART_INF_F;
+#pragma unroll
+                  for (int w = 0; w < 4; ++w)
+                    if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][rb][w][k]);
+                  keep[q][k] = (mx * p.sigma) >= thr[q];
+                }
+            } else {
+              // lambda: sub-blocks in ascending key order; the running max of
+              // a row moves only with the blocks it keeps.
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                if (k >= KS) break;
+                const float rmk = (k == 0) ? rm0 : rm1;
+                bool need_vote = false;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) need_vote |= (cls[q][k] == 1);
+                if (need_vote) {
+                  const bool want =
+                      rvalid && cls[myqs][k] == 1 && ((rmk - m_true) * p.sigma >= p.log_lambda);
+                  const unsigned any = __ballot_sync(0xffffffffu, want);
+                  const int rb = nsync & 1;
+                  if (lane == 0) {
+                    c->red[s][rb][wq][k] = any ? 1.f : 0.f;
+                    mbar_arrive(&c->wg[s][rb]);
+                  }
+                  if (!(ok = wait_bar(&c->wg[s][rb], (nsync >> 1) & 1, abort, p.err, ERR_WAIT_WG)))
+                    break;
+                  ++nsync;
+#pragma unroll
+                  for (int q = 0; q < 2; ++q) {
+                    if (cls[q][k] != 1) continue;
+                    bool kp = false;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                      if (QS == 1 || (w >> 1) == q) kp |= (c->red[s][rb][w][k] != 0.f);
+                    keep[q][k] = kp;
+                  }
+                }
+                if (keep[myqs][k]) m_true = fmaxf(m_true, rmk);
+              }
+              if (!ok) break;
+            }
+          }
+          uint32_t decbits = 0;
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              if (keep[q][k]) decbits |= 1u << (q * 2 + k);
+          if (GATING && row == 0) {
+            c->dec[s][tb] = decbits;
+            mbar_arrive(&c->dec_full[s][tb]);
+          }
+
+          // ---- bookkeeping: bitmap words and block counts
+          if (leader && my_i * p.Bq < len) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int cl = cls[myqs][k];
+              if (cl == 0) continue;
+              const int j = (J * TILE) / p.Bk + k;
+              if (cl == 1) {
+                ++cnt_cand;
+                cnt_kept += keep[myqs][k] ? 1 : 0;
+              } else {
+                ++cnt_diag;
+              }
+              if (bm_on) {
+                if ((j >> 5) != bm_idx) {
+                  p.bitmap[bm_row + bm_idx] = bm_word;
+                  bm_idx = j >> 5;
+                  bm_word = 0;
+                }
+                if (keep[myqs][k]) bm_word |= 1u << (j & 31);
+              }
+            }
+          }
+
+          // ---- online softmax over the kept sub-blocks of this slot
+          if (decbits != 0u) {
+            const bool k0 = keep[myqs][0];
+            const bool k1 = (KS == 1) ? k0 : keep[myqs][1];
+            float rmk = -CUDART_INF_F;
+            if (k0) rmk = fmaxf(rmk, rm0);
+            if (k1) rmk = fmaxf(rmk, rm1);
+            const float m_new = fmaxf(m_used, rmk);
+            const bool resc = (m_new - m_used) * p.sigma_log2 > RESCALE_LOG2;
+            float alpha = 1.f;
+            if (resc) {
+              alpha = ex2_approx((m_used - m_new) * p.sigma_log2);
+              m_used = m_new;
+              l *= alpha;
+            }
+            if (o_init && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+              for (int q = 0; q < D / 32; ++q) {
+                uint32_t orr[32];
+                tmem_ld32(tO + q * 32, orr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                tmem_st32(tO + q * 32, orr);
+              }
+            }
+            // Pass 2: P = exp2(sigma*log2e*(S - m)) for the kept, visible
+            // entries, packed as bf16 pairs into the first 64 columns of the
+            // S region (half hf of S -> P columns [32 hf, 32 hf + 32); those
+            // S columns were already read).
+            const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * p.sigma_log2;
+            float lsum = 0.f;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const bool kk = (hf == 0) ? k0 : k1;
+              uint32_t sr[2][32];
+              tmem_ld32(tS + hf * 64, sr[0]);
+              tmem_ld32(tS + hf * 64 + 32, sr[1]);
+              tmem_wait_ld();
+              uint32_t pk[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int cc = hf * 64 + 2 * e;
+                const bool vis0 = kk && !(diag_tile && cc > row);
+                const bool vis1 = kk && !(diag_tile && cc + 1 > row);
+                const float x0 = __uint_as_float(sr[(2 * e) >> 5][(2 * e) & 31]);
+                const float x1 = __uint_as_float(sr[(2 * e + 1) >> 5][(2 * e + 1) & 31]);
+                const float p0 = vis0 ? ex2_approx(fmaf(x0, p.sigma_log2, -mb)) : 0.f;
+                const float p1 = vis1 ? ex2_approx(fmaf(x1, p.sigma_log2, -mb)) : 0.f;
+                lsum += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
+              }
+              tmem_st32(tS + hf * 32, pk);
+            }
+            l += lsum;
+            tmem_wait_st();
+            o_init = true;
+          }
+          tc_fence_before();
+          mbar_arrive(&c->p_full[s]);
+        }
+      }
+      if (!ok) break;
+
+      if constexpr (!CALIB) {
+        // ---- epilogue: O / l -> bf16, log-sum-exp, bitmap tail
+        if (bm_on) {
+          p.bitmap[bm_row + bm_idx] = bm_word;
+          for (int w = bm_idx + 1; w < p.words; ++w) p.bitmap[bm_row + w] = 0u;
+        }
+        if (!(ok = wait_bar(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL))) break;
+        tc_fence_after();
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        __nv_bfloat16* orow =
+            p.o + (long long)si.w * p.o_sb + (long long)h * p.o_sh + (long long)(si.x + qpos) * p.o_st;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t orr[32];
+          tmem_ld32(tO + q * 32, orr);
+          tmem_wait_ld();
+          if (rvalid) {
+            uint4 pk[4];
+            uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pw[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
+                                  __uint_as_float(orr[2 * e + 1]) * inv_l);
+            uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = pk[e];
+          }
+        }
+        if (p.lse != nullptr && rvalid)
+          p.lse[(long long)h * p.lse_rows +
+                (p.varlen ? (long long)si.x : (long long)si.w * p.batch_len) + qpos] =
+              m_used * p.sigma + logf(l);
+        tc_fence_before();
+        mbar_arrive(&c->o_empty[s]);
+      }
+    }
+    if (p.counts != nullptr && (cnt_cand | cnt_diag) != 0ull) {
+      atomicAdd(&p.counts[0], cnt_kept);
+      atomicAdd(&p.counts[1], cnt_cand);
+      atomicAdd(&p.counts[2], cnt_diag);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, LY::NCOLS);
+  }
+}
+
+}  // namespace bsfa

@@ -1,0 +1,19 @@
+// bsfa_launch.h -- internal declarations shared by the host API and the
+// translation units that instantiate the attention kernel.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "bsfa_fwd.cuh"
+
+namespace bsfa {
+
+struct Maps {
+  CUtensorMap q, k, v;
+};
+
+// Launches bsfa_fwd_kernel<D, NQ, GATING, CALIB> with its shared-memory size.
+template <int D, int NQ, bool GATING, bool CALIB>
+cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream);
+
+}  // namespace bsfa

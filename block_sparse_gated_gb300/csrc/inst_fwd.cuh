@@ -1,0 +1,27 @@
+// inst_fwd.cuh -- explicit instantiation helper for the attention kernel.
+#pragma once
+#include "bsfa_launch.h"
+
+namespace bsfa {
+
+template <int D, int NQ, bool GATING, bool CALIB>
+cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream) {
+  using LY = Layout<D, NQ, CALIB>;
+  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB>;
+  static bool configured[64] = {};  // the attribute is per device; set once on each
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = true;
+  }
+  fn<<<grid, LY::NTHREADS, LY::BYTES, stream>>>(m.q, m.k, m.v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace bsfa
+
+#define BSFA_INSTANTIATE(D, NQ, G, C) \
+  template cudaError_t bsfa::launch_fwd<D, NQ, G, C>(const Maps&, const DevParams&, int, cudaStream_t);

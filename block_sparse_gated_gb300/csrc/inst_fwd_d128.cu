@@ -1,0 +1,8 @@
+// Attention kernels for head_dim 128 (gated and gate-compiled-out).
+#include "inst_fwd.cuh"
+namespace bsfa {
+BSFA_INSTANTIATE(128, 2, true, false)
+BSFA_INSTANTIATE(128, 1, true, false)
+BSFA_INSTANTIATE(128, 2, false, false)
+BSFA_INSTANTIATE(128, 1, false, false)
+}  // namespace bsfa

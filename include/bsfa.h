@@ -1,0 +1,179 @@
+/*
+ * bsfa.h -- C ABI of libbsfa.so: block-sparse gated causal prefill attention
+ * (Block Sparse Flash Attention form) for NVIDIA GB300 (sm_103a).
+ *
+ * Operations and where they are defined:
+ *
+ *   bsfa_prefill_fwd   "Block Sparse Flash Attention" (papernotes.org note on
+ *                      arXiv 2512.07011), Key Designs 2 "Exact-Score Gating"
+ *                      (displayed equation: s_max(i,j) over the whole
+ *                      Bq x Bk tile of QK^T/sqrt(d); keep iff s_max >= T) and
+ *                      Key Designs 3 "Selective Streaming Aggregation"
+ *                      (a rejected tile gets no V load, no exp, no P.V and no
+ *                      update of the running max, the normaliser or the output
+ *                      accumulator; the output is renormalised over the
+ *                      retained blocks).  The lambda-relative mode follows
+ *                      "Skipping attention blocks was the easy part"
+ *                      (yash-agarwal.org, BLASST), section "Vote, then skip".
+ *   bsfa_calibrate     same BSFA note, Key Designs 1 "Offline Threshold
+ *                      Calibration": per head and query block, the k-th
+ *                      largest maximum over the visible off-diagonal key
+ *                      blocks, averaged over calibration samples; -inf when
+ *                      fewer than k candidates exist.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers unless a parameter says "host".
+ *     The caller owns every buffer; the library never allocates device memory
+ *     (scratch comes from the caller's workspace).
+ *   - Calls are asynchronous on `stream` and never synchronise the host,
+ *     except bsfa_device_error which synchronises `stream` by design.
+ *   - Errors that the host can detect are returned before anything is
+ *     launched.  A device-side wait that ran out of time (a hang guard, never
+ *     expected in a correct run) sets a device error word; it is reported by
+ *     bsfa_device_error.
+ *   - No C++ exception crosses this boundary.
+ *
+ * Block geometry (all positions local to a sequence):
+ *   query block i covers rows [i*Bq, min((i+1)*Bq, L)); key block j covers
+ *   keys [j*Bk, min((j+1)*Bk, L)).  Key block j is a CANDIDATE for query
+ *   block i when (j+1)*Bk <= i*Bq (every key precedes every row: the tile lies
+ *   strictly below the causal diagonal).  A visible block that is not a
+ *   candidate belongs to the diagonal region: it is always kept and the
+ *   causal mask is applied to it.
+ */
+#ifndef BSFA_H
+#define BSFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* bsfa_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  BSFA_OK = 0,
+  BSFA_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, GQA mismatch, bad stride */
+  BSFA_ERR_UNSUPPORTED = 2,   /* head_dim / block sizes / alignment not supported */
+  BSFA_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+  BSFA_ERR_DEVICE_TIMEOUT = 4,/* a device-side wait exceeded its bound */
+  BSFA_ERR_WORKSPACE = 5      /* workspace pointer null/misaligned or too small */
+} bsfa_status;
+
+typedef enum {
+  BSFA_GATE_THRESHOLD = 0, /* keep candidate (i,j) iff sigma*max(QK^T tile) >= T[h][min(i,nT-1)] */
+  BSFA_GATE_LAMBDA = 1,    /* skip candidate iff for every row r: sigma*(rowmax_r - m_r) < log_lambda,
+                              m_r = exact running max over kept blocks, blocks in ascending key
+                              order with the diagonal region last */
+  BSFA_GATE_NONE = 2       /* dense causal attention: a kernel built with the gate compiled out
+                              (the zero-skip overhead reference) */
+} bsfa_gate_mode;
+
+/*
+ * Parameters of one prefill call.  Q, K, V, O are bf16 with the head
+ * dimension contiguous; every other dimension is addressed through strides
+ * given in ELEMENTS as {batch, head, token}.  Two layouts are accepted:
+ *   - batched  (cu_seqlens == NULL): `batch` sequences of `seqlen` tokens,
+ *     e.g. [B, H, L, d] or [B, L, H, d];
+ *   - varlen   (cu_seqlens != NULL): `batch` sequences packed along tokens,
+ *     `seqlen` = total packed tokens, sequence b owns tokens
+ *     [cu_seqlens[b], cu_seqlens[b+1]); the batch stride is ignored.
+ * Strides must be multiples of 8 elements (16 bytes) and the base pointers
+ * 16-byte aligned (TMA requirement).  q-head h reads KV head h / (Hq/Hkv).
+ */
+typedef struct {
+  const void* q;              /* bf16 [.., Hq, .., d]  */
+  const void* k;              /* bf16 [.., Hkv, .., d] */
+  const void* v;              /* bf16 [.., Hkv, .., d] */
+  void* o;                    /* bf16, same shape as q; rows past a sequence end untouched */
+  int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3]; /* {batch, head, token} */
+  int batch;                  /* number of sequences (>= 0; 0 is a no-op) */
+  int num_heads_q;            /* Hq */
+  int num_heads_kv;           /* Hkv, Hq % Hkv == 0 */
+  int seqlen;                 /* tokens per sequence (batched) or total tokens (varlen) */
+  int head_dim;               /* d: 64 or 128 */
+  const int32_t* cu_seqlens;  /* device int32 [batch+1], nullable (batched layout) */
+  int max_seqlen;             /* varlen: an upper bound on every sequence length */
+  int block_q, block_k;       /* semantic gate blocks Bq, Bk: each 64 or 128 */
+  float softmax_scale;        /* sigma; <= 0 selects 1/sqrt(d) */
+  int mode;                   /* bsfa_gate_mode */
+  const float* thresholds;    /* device fp32 [Hq][thresholds_nq] (THRESHOLD mode): the
+                                 slice for one (budget, layer); natural-log units of the
+                                 scaled scores; -inf keeps everything */
+  int thresholds_nq;          /* nT >= 1; query blocks i >= nT use T[h][nT-1] */
+  float log_lambda;           /* natural log of lambda (LAMBDA mode) */
+  uint32_t* kept_bitmap;      /* nullable device output, see bsfa_bitmap_shape: bit j of
+                                 row (h, row_base(b) + i) = keep(i,j); diagonal-region bits
+                                 are 1; invisible blocks 0; every word of every row written */
+  float* lse;                 /* nullable device fp32 output [Hq][rows]: natural-log
+                                 log-sum-exp of the kept scaled scores, row = b*seqlen+pos
+                                 (batched) or cu_seqlens[b]+pos (varlen) */
+  unsigned long long* block_counts; /* nullable device u64[3], overwritten: kept candidate
+                                 blocks, visible candidate blocks, diagonal-region blocks
+                                 (semantic Bq x Bk blocks, all heads and sequences) */
+  void* workspace;            /* device scratch, >= bsfa_prefill_workspace_size bytes,
+                                 256-byte aligned; its contents are not preserved */
+  size_t workspace_bytes;
+} bsfa_fwd_params;
+
+/* Bytes of workspace bsfa_prefill_fwd needs for these parameters (reads the
+ * shape fields only).  Returns 0 for invalid parameters. */
+size_t bsfa_prefill_workspace_size(const bsfa_fwd_params* p);
+
+/* Shape of the optional kept-block bitmap: *rows = Hq * sum_b ceil(L_b/Bq) is
+ * not knowable on the host in varlen mode without the lengths, so the host
+ * passes an upper bound through the call below:
+ *   words_per_row = ceil(ceil(max_len / Bk) / 32), max_len = seqlen (batched)
+ *   or max_seqlen (varlen);
+ *   rows_per_head = batch * ceil(seqlen / Bq) (batched) or
+ *   sum_b ceil(L_b / Bq) (varlen, computed by the caller from its lengths);
+ *   row_base(b) = sum_{b' < b} ceil(L_b' / Bq).
+ * Returns BSFA_OK or BSFA_ERR_INVALID_ARG. */
+bsfa_status bsfa_bitmap_words_per_row(const bsfa_fwd_params* p, int* words_per_row);
+
+/* Gated causal prefill.  Validates `p`, then enqueues on `stream` a small
+ * scheduling kernel and the persistent attention kernel.  Asynchronous.
+ * Errors: BSFA_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE before any launch;
+ * BSFA_ERR_CUDA if a launch or descriptor encode fails. */
+bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream);
+
+/*
+ * Offline threshold calibration for one layer and a set of budgets.
+ *   q_samples / k_samples: HOST arrays of n_samples DEVICE pointers to bf16
+ *     tensors of one sample each, layout [H, L, d] addressed by the strides
+ *     {head, token} in elements (d contiguous), equal L for every sample.
+ *   ks: HOST array of n_k budgets (each >= 1).
+ *   thresholds_out: device fp32 [n_k][Hq][ceil(L/Bq)], overwritten with the
+ *     mean over samples of the k-th largest candidate block maximum (scaled
+ *     by sigma), -inf where a sample has fewer than k candidates.
+ *   workspace: >= bsfa_calibrate_workspace_size(...) bytes, 256-byte aligned.
+ * Asynchronous on `stream`.
+ */
+size_t bsfa_calibrate_workspace_size(int num_heads_q, int seqlen, int block_q, int block_k);
+
+bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_samples,
+                           int n_samples, int num_heads_q, int num_heads_kv, int seqlen,
+                           int head_dim, const int64_t q_stride[2], const int64_t k_stride[2],
+                           int block_q, int block_k, float softmax_scale,
+                           const int* ks, int n_k, float* thresholds_out,
+                           void* workspace, size_t workspace_bytes, bsfa_stream_t stream);
+
+/* Synchronises `stream`, then reports (and clears) the device error word set
+ * by a kernel whose bounded wait ran out.  *code receives the raw word (0 if
+ * none).  Returns BSFA_ERR_DEVICE_TIMEOUT if it was set, BSFA_ERR_CUDA if the
+ * synchronisation failed, else BSFA_OK. */
+bsfa_status bsfa_device_error(bsfa_stream_t stream, unsigned int* code);
+
+/* Static description of a status code. */
+const char* bsfa_status_string(bsfa_status s);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int bsfa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSFA_H */

@@ -1,0 +1,515 @@
+"""Benchmark of the gated causal prefill path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu] [--no-sweep]
+
+Default workload: one Llama-3.1-8B attention layer at L = 131072 (32 query
+heads, 8 KV heads, d = 128, Bq = Bk = 128) with a 256-token sink and 64
+needle blocks per KV head; thresholds calibrated by bsfa_calibrate on four
+seeded 64K inputs for budgets k = 32, 128, 512.  One step = the three budget
+slices run back to back.  Inputs (Q 1 GiB, K and V 256 MiB each) exceed the
+129 MB L2, so no flush is needed between iterations.
+
+Prints ONE JSON line (rank 0).  value = effective TFLOP/s over the step,
+effective FLOPs = 2*Bq*Bk*d * (visible blocks + kept blocks).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("prefill attention ms/layer & effective TFLOPS (frac of bf16 peak) at 128K vs "
+          "skip rate")
+UNIT = "TFLOP/s (effective)"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, f[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(n)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+def _cfg(name):
+    from block_sparse_gated_gb300 import workloads as wl
+    return wl.WORKLOADS[name]
+
+
+def build_workload(name, device):
+    """Inputs on the device and the calibrated threshold slices (GPU path)."""
+    import torch
+
+    import block_sparse_gated_gb300 as bsfa
+    from block_sparse_gated_gb300 import workloads as wl
+    cfg = _cfg(name)
+    Hq, Hkv, d, Bq, Bk = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["Bq"], cfg["Bk"]
+    cal = []
+    for n in range(cfg["n_cal"]):
+        x = wl.layer_inputs(Hq, Hkv, cfg["cal_L"], d, wl.cal_seed(cfg["index"], n), device,
+                            with_v=False, sink_tokens=cfg["sink_tokens"],
+                            needles=cfg["cal_needles"], block=Bk)
+        cal.append((x.q, x.k))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    T = bsfa.calibrate([c[0] for c in cal], [c[1] for c in cal], cfg["ks"], block_q=Bq, block_k=Bk)
+    ev1.record()
+    torch.cuda.synchronize()
+    cal_ms = ev0.elapsed_time(ev1)
+    nq_cal = T.shape[2]
+    cal_flops = cfg["n_cal"] * Hq * 2.0 * Bq * Bk * d * (nq_cal * (nq_cal + 1) / 2)
+    del cal
+    x = wl.layer_inputs(Hq, Hkv, cfg["L"], d, wl.eval_seed(cfg["index"]), device,
+                        sink_tokens=cfg["sink_tokens"], needles=cfg["needles"], block=Bk)
+    torch.cuda.synchronize()
+    return {"cfg": cfg, "q": x.q, "k": x.k, "v": x.v, "T": T, "cal_ms": cal_ms,
+            "cal_tflops": cal_flops / (cal_ms * 1e-3) / 1e12,
+            "gen_s": time.perf_counter() - t0}
+
+
+def effective_flops(counts, Bq, Bk, d):
+    kept_c, cand, diag = counts
+    return 2.0 * Bq * Bk * d * ((cand + diag) + (kept_c + diag))
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_gated_gb300 as bsfa
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peak_burst, peak_sust, peak_kind = _peaks()
+    W = build_workload(args.workload, dev)
+    cfg = W["cfg"]
+    Hq, d, Bq, Bk, L = cfg["Hq"], cfg["d"], cfg["Bq"], cfg["Bk"], cfg["L"]
+    q, k, v, T = W["q"][None], W["k"][None], W["v"][None], W["T"]
+    ks = cfg["ks"]
+    slices = [T[i].contiguous() for i in range(len(ks))]
+    outs = [torch.empty_like(q) for _ in ks]
+    counts = [torch.zeros(3, dtype=torch.int64, device=dev) for _ in ks]
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(i):
+        bsfa.prefill(q, k, v, block_q=Bq, block_k=Bk, mode="threshold", thresholds=slices[i],
+                     out=outs[i], workspace=ws, stream=stream)
+
+    # counts: one untimed pass with counters on
+    for i in range(len(ks)):
+        r = bsfa.prefill(q, k, v, block_q=Bq, block_k=Bk, mode="threshold",
+                         thresholds=slices[i], out=outs[i], workspace=ws, return_counts=True)
+        counts[i] = r["counts"]
+    torch.cuda.synchronize()
+    cnts = [c.cpu().tolist() for c in counts]
+    flops = [effective_flops(c, Bq, Bk, d) for c in cnts]
+
+    for _ in range(args.warmup):
+        for i in range(len(ks)):
+            call(i)
+    torch.cuda.synchronize()
+    starts = [[torch.cuda.Event(enable_timing=True) for _ in ks] for _ in range(args.steps)]
+    ends = [[torch.cuda.Event(enable_timing=True) for _ in ks] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_start.record(stream)
+        for s in range(args.steps):
+            for i in range(len(ks)):
+                starts[s][i].record(stream)
+                call(i)
+                ends[s][i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = clk.summary()
+    total_ms = t_start.elapsed_time(t_end)
+    ms_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    per_slice_ms = [statistics.mean(starts[s][i].elapsed_time(ends[s][i]) for s in range(args.steps))
+                    for i in range(len(ks))]
+    step_flops = sum(flops)
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    launch_achieved = sum(flops) / (sum(per_slice_ms) * 1e-3) / 1e12
+    slices_out = []
+    for i, kk in enumerate(ks):
+        kc, cand, diag = cnts[i]
+        tf = flops[i] / (per_slice_ms[i] * 1e-3) / 1e12
+        slices_out.append({
+            "k": kk, "ms_per_layer": round(per_slice_ms[i], 3),
+            "skip_rate": round(1.0 - kc / cand, 4) if cand else 0.0,
+            "density": round((kc + diag) / (cand + diag), 4),
+            "effective_tflops": round(tf, 1),
+            "frac_of_burst_peak": round(tf / peak_burst, 4),
+            "frac_of_sustained_peak": round(tf / peak_sust, 4)})
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; Llama-3.1-8B attention shapes; no dataset)",
+        "config": {"workload": args.workload, "Hq": Hq, "Hkv": cfg["Hkv"], "d": d, "L": L,
+                   "Bq": Bq, "Bk": Bk, "budgets_k": ks, "calibration": f"{cfg['n_cal']} x "
+                   f"{cfg['cal_L']} tokens", "l2": "inputs larger than L2 (Q 1 GiB, K/V 256 MiB)",
+                   "parallelism": f"replica x{world}"},
+        "slices": slices_out,
+        "roofline": {"bound": "tensor", "achieved": round(launch_achieved, 1),
+                     "peak": peak_sust, "unit": "TFLOP/s",
+                     "frac": round(launch_achieved / peak_sust, 4),
+                     "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
+                     "frac_of_burst": round(launch_achieved / peak_burst, 4),
+                     "traffic": None},
+        "clocks": clocks,
+        "gpu_launches": 2 * len(ks) * args.steps,
+        "calibrate": {"ms": round(W["cal_ms"], 3), "samples": cfg["n_cal"],
+                      "tflops_qk": round(W["cal_tflops"], 1)},
+    }
+
+    if not args.no_sweep and rank == 0:
+        result["lambda_sweep"] = lambda_sweep(dev, args)
+    if not args.no_e2e:
+        result["e2e"] = e2e(q, k, v, slices, flops, Bq, Bk, args, dev)
+    if not args.no_cpu and rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(args.workload, W, cnts)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def e2e(q, k, v, slices, flops, Bq, Bk, args, dev):
+    """Same metric through the public API with host buffers: per step the
+    pinned Q/K/V go host->device, the three slices run, and the three outputs
+    come back device->host."""
+    import torch
+
+    import block_sparse_gated_gb300 as bsfa
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in slices]
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    od = [torch.empty_like(q) for _ in slices]
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        for i, T in enumerate(slices):
+            bsfa.prefill(qd, kd, vd, block_q=Bq, block_k=Bk, mode="threshold", thresholds=T,
+                         out=od[i], workspace=ws)
+            oh[i].copy_(od[i], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 3))
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = sum(t.numel() * t.element_size() for t in oh)
+    return {"value": round(sum(flops) / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def lambda_sweep(dev, args):
+    """lambda gate at 64K: time vs dialled skip rate, plus the same kernel with
+    the gate compiled out (0-skip overhead)."""
+    import torch
+
+    import block_sparse_gated_gb300 as bsfa
+    from block_sparse_gated_gb300 import workloads as wl
+    cfg = _cfg("lambda-sweep-L65536")
+    Hq, Hkv, d, L, B = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["L"], cfg["Bk"]
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    reps = 3
+    rows = []
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    for n, r in enumerate(cfg["skip_rates"]):
+        x = wl.layer_inputs(Hq, Hkv, L, d, wl.eval_seed(cfg["index"], n), dev, skip_rate=r, block=B)
+        q, k, v = x.q[None], x.k[None], x.v[None]
+        out = torch.empty_like(q)
+        ll = cfg["log_lambda"] if r > 0 else -math.inf
+        res = bsfa.prefill(q, k, v, mode="lambda", log_lambda=ll, out=out, workspace=ws,
+                           return_counts=True)
+        torch.cuda.synchronize()
+        kc, cand, diag = res["counts"].cpu().tolist()
+        ms = timed(lambda: bsfa.prefill(q, k, v, mode="lambda", log_lambda=ll, out=out,
+                                        workspace=ws))
+        row = {"target_skip": r, "log_lambda": ll if math.isfinite(ll) else "-inf",
+               "measured_skip": round(1 - kc / cand, 4), "ms": round(ms, 3),
+               "effective_tflops": round(effective_flops((kc, cand, diag), B, B, d) /
+                                         (ms * 1e-3) / 1e12, 1)}
+        if r == 0:
+            thr = torch.full((Hq, 1), -math.inf, device=dev)
+            row["ms_threshold_minus_inf"] = round(timed(lambda: bsfa.prefill(
+                q, k, v, mode="threshold", thresholds=thr, out=out, workspace=ws)), 3)
+            row["ms_gate_compiled_out"] = round(timed(lambda: bsfa.prefill(
+                q, k, v, mode="none", out=out, workspace=ws)), 3)
+        rows.append(row)
+        del x, q, k, v, out
+    base = rows[0]["ms_gate_compiled_out"]
+    times = [r_["ms"] for r_ in rows]
+    return {"workload": "lambda-sweep-L65536", "rows": rows,
+            "zero_skip_overhead_lambda": round(rows[0]["ms"] / base - 1, 4),
+            "zero_skip_overhead_threshold": round(rows[0]["ms_threshold_minus_inf"] / base - 1, 4),
+            "monotonic": all(a > b for a, b in zip(times, times[1:]))}
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(q_heads, k_heads, v_heads, heads, T_rows, blocks, Bq, Bk, sigma):
+    """Time the oracle on sampled (head, query block) units.  Returns
+    (effective FLOPs, seconds, n_blocks)."""
+    from oracle import bsfa_oracle as orc
+    d = q_heads[heads[0]].shape[1]
+    F = 2.0 * Bq * Bk * d
+    fl, t0 = 0.0, time.perf_counter()
+    for h, i in blocks:
+        r = orc.query_block(q_heads[h], k_heads[h], v_heads[h], i, Bq=Bq, Bk=Bk, sigma=sigma,
+                            mode="threshold", T_hi=T_rows[(h, i)])
+        fl += F * (len(r["keep"]) + sum(r["keep"].values()))
+    return fl, time.perf_counter() - t0, len(blocks)
+
+
+def _sample_blocks(n_q, nT, heads, per_head, seed):
+    import random
+    rnd = random.Random(seed)
+    out = []
+    for h in heads:
+        fixed = sorted({0, nT - 1, min(nT, n_q - 1), n_q - 1})
+        extra = rnd.sample(range(n_q), per_head)
+        out += [(h, i) for i in sorted(set(fixed + extra))]
+    return out
+
+
+def _oracle_inputs(name, W=None, heads=(0, 17)):
+    """fp64 host copies of the sampled heads (and their KV heads), and oracle
+    thresholds for the sampled rows computed from the calibration recipe."""
+    import numpy as np
+    import torch
+
+    from block_sparse_gated_gb300 import workloads as wl
+    from oracle import bsfa_oracle as orc
+    cfg = _cfg(name)
+    Hq, Hkv, d, Bq, Bk = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["Bq"], cfg["Bk"]
+    g = Hq // Hkv
+    dev = W["q"].device if W is not None else "cpu"
+    if W is None:
+        x = wl.layer_inputs(Hq, Hkv, cfg["L"], d, wl.eval_seed(cfg["index"]), "cpu",
+                            sink_tokens=cfg["sink_tokens"], needles=cfg["needles"], block=Bk)
+        q, k, v = x.q, x.k, x.v
+    else:
+        q, k, v = W["q"], W["k"], W["v"]
+    qh = {h: q[h].to("cpu", torch.float64).numpy() for h in heads}
+    kh = {h: k[h // g].to("cpu", torch.float64).numpy() for h in heads}
+    vh = {h: v[h // g].to("cpu", torch.float64).numpy() for h in heads}
+    return cfg, qh, kh, vh
+
+
+def _oracle_thresholds(cfg, heads, blocks, device):
+    """Oracle calibration restricted to the table entries the sampled blocks
+    read (k = the smallest budget), from the calibration recipe's inputs."""
+    import numpy as np
+    import torch
+
+    from block_sparse_gated_gb300 import workloads as wl
+    from oracle import bsfa_oracle as orc
+    Hq, Hkv, d, Bq, Bk = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["Bq"], cfg["Bk"]
+    g = Hq // Hkv
+    nT = (cfg["cal_L"] + Bq - 1) // Bq
+    rows = sorted({(h, min(i, nT - 1)) for h, i in blocks})
+    acc = {r: 0.0 for r in rows}
+    for n in range(cfg["n_cal"]):
+        x = wl.layer_inputs(Hq, Hkv, cfg["cal_L"], d, wl.cal_seed(cfg["index"], n), device,
+                            with_v=False, sink_tokens=cfg["sink_tokens"],
+                            needles=cfg["cal_needles"], block=Bk)
+        for h in heads:
+            q64 = x.q[h].to("cpu", torch.float64).numpy()
+            k64 = x.k[h // g].to("cpu", torch.float64).numpy()
+            for (hh, t) in rows:
+                if hh != h:
+                    continue
+                c = orc.candidate_maxima(q64, k64, t, Bq, Bk, 1.0 / math.sqrt(d))
+                acc[(h, t)] += orc.kth_largest(c, cfg["ks"][0])
+        del x
+    return {(h, i): acc[(h, min(i, nT - 1))] / cfg["n_cal"] for h, i in blocks}, nT
+
+
+def cpu_baseline(name, W, cnts=None):
+    """The oracle on a bounded sample of the same workload on the host cores."""
+    cfg, qh, kh, vh = _oracle_inputs(name, W)
+    heads = sorted(qh)
+    n_q = (cfg["L"] + cfg["Bq"] - 1) // cfg["Bq"]
+    nT = (cfg["cal_L"] + cfg["Bq"] - 1) // cfg["Bq"]
+    blocks = _sample_blocks(n_q, nT, heads, 3, 0)
+    T_rows, _ = _oracle_thresholds(cfg, heads, blocks, W["q"].device)
+    fl, sec, nb = oracle_sample(qh, kh, vh, heads, T_rows, blocks, cfg["Bq"], cfg["Bk"],
+                                1.0 / math.sqrt(cfg["d"]))
+    return {"value": round(fl / sec / 1e12, 5), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{nb} (head, query-block) units of the 128K layer (heads {heads}, "
+                      f"first/last/calibrated-boundary blocks + random), k={cfg['ks'][0]} slice, "
+                      f"fp64 numpy; {sec:.1f} s"}
+
+
+# ----------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    """The fp64 oracle as it stands on the host cores: same metric and unit,
+    each step a bounded sample of the workload's (head, query-block) units."""
+    if rank != 0:
+        return
+    cfg, qh, kh, vh = _oracle_inputs(args.workload, None)
+    heads = sorted(qh)
+    n_q = (cfg["L"] + cfg["Bq"] - 1) // cfg["Bq"]
+    nT = (cfg["cal_L"] + cfg["Bq"] - 1) // cfg["Bq"]
+    steps = [_sample_blocks(n_q, nT, heads[:1], 1, 100 + s) for s in range(args.warmup + args.steps)]
+    allb = sorted({b for st in steps for b in st})
+    T_rows, _ = _oracle_thresholds(cfg, heads[:1], allb, "cpu")
+    for st in steps[:args.warmup]:
+        oracle_sample(qh, kh, vh, heads, T_rows, st[:1], cfg["Bq"], cfg["Bk"], 1 / math.sqrt(cfg["d"]))
+    tot_f, tot_s, tot_b = 0.0, 0.0, 0
+    for st in steps[args.warmup:]:
+        f, s, b = oracle_sample(qh, kh, vh, heads, T_rows, st, cfg["Bq"], cfg["Bk"],
+                                1 / math.sqrt(cfg["d"]))
+        tot_f, tot_s, tot_b = tot_f + f, tot_s + s, tot_b + b
+    val = tot_f / tot_s / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 5), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * tot_s / args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "sample": "per step: query blocks of head 0"},
+            "cpu_baseline": {"value": round(val, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{tot_b} (head, query-block) units over {args.steps} "
+                                       f"steps, fp64 numpy"},
+            "e2e": {"value": round(val, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b-L131072")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

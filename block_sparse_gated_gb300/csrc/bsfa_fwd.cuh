@@ -74,7 +74,6 @@ struct Ctrl {
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[NQ], p_full[NQ], o_full[NQ], o_empty[NQ];
   uint64_t dec_full[NQ][2];
-  uint64_t wg[NQ][2];
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t dec[NQ][2];
@@ -125,10 +124,25 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > WAIT_TIMEOUT_NS / 20) return;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Barrier over the `n` threads of a warpgroup that also ANDs a predicate:
+// every thread learns whether all of them are still running.
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
 // Semantic block class of key block j for query block i (length-L sequence):
@@ -173,8 +187,6 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       mbar_init(&c->o_empty[s], 128);
       mbar_init(&c->dec_full[s][0], 1);
       mbar_init(&c->dec_full[s][1], 1);
-      mbar_init(&c->wg[s][0], 4);
-      mbar_init(&c->wg[s][1], 4);
     }
     mbar_init(&c->q_empty, 1);
     for (int i = 0; i < KST; ++i) {
@@ -393,13 +405,16 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     const int s = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
+    const uint32_t bar_id = 1 + s;  // named barrier of this warpgroup
     const uint32_t tlane = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + tlane + s * 128;
     const uint32_t tO = tmem + tlane + NQ * 128 + s * D;
     const int QS = TILE / p.Bq, KS = TILE / p.Bk;
+    const bool simple = (QS == 1 && KS == 1);  // one semantic block per 128x128 tile
     const int myqs = (p.Bq == 64) ? (row >> 6) : 0;
     const bool leader = (row % p.Bq) == 0;  // first row of its semantic query block
-    uint32_t tc = 0, uc = 0, nsync = 0;
+    const float sc = p.sigma_log2;
+    uint32_t tc = 0, uc = 0;
     bool ok = true;
     unsigned long long cnt_kept = 0, cnt_cand = 0, cnt_diag = 0;
 
@@ -427,63 +442,85 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 
       for (int J = 0; J < nkt; ++J, ++tc) {
         const int tb = tc & 1;
-        if (!(ok = wait_bar(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL))) break;
+        const bool okl = wait_bar(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL);
         tc_fence_after();
-        // Pass 1: row maxima of the two 64-key halves (the causal mask only
-        // reaches into the last tile, J == I, where key column c > row is
-        // invisible).  S stays in TMEM; pass 2 reads it again.
-        const bool diag_tile = (J == I);
+        const bool diag_tile = (J == I);  // keys beyond a row exist only in the last tile
+
+        // ---- pass 1: row maxima of the two 64-key halves of S
         float rm0 = -CUDART_INF_F, rm1 = -CUDART_INF_F;
+        if (okl) {
+          uint32_t sr[4][32];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t sr[2][32];
-          tmem_ld32(tS + hf * 64, sr[0]);
-          tmem_ld32(tS + hf * 64 + 32, sr[1]);
+          for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
           tmem_wait_ld();
-          float mx = -CUDART_INF_F;
+          if (!diag_tile) {
+            rm0 = max3f(__uint_as_float(sr[0][0]), __uint_as_float(sr[0][1]),
+                        __uint_as_float(sr[0][2]));
+            rm1 = max3f(__uint_as_float(sr[2][0]), __uint_as_float(sr[2][1]),
+                        __uint_as_float(sr[2][2]));
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const float x = __uint_as_float(sr[e >> 5][e & 31]);
-            mx = (diag_tile && (hf * 64 + e) > row) ? mx : fmaxf(mx, x);
+            for (int e = 3; e < 63; e += 2) {
+              rm0 = max3f(rm0, __uint_as_float(sr[e >> 5][e & 31]),
+                          __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]));
+              rm1 = max3f(rm1, __uint_as_float(sr[2 + (e >> 5)][e & 31]),
+                          __uint_as_float(sr[2 + ((e + 1) >> 5)][(e + 1) & 31]));
+            }
+            rm0 = fmaxf(rm0, __uint_as_float(sr[1][31]));
+            rm1 = fmaxf(rm1, __uint_as_float(sr[3][31]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 128; ++e) {
+              const float x = (e > row) ? -CUDART_INF_F : __uint_as_float(sr[e >> 5][e & 31]);
+              if (e < 64) rm0 = fmaxf(rm0, x); else rm1 = fmaxf(rm1, x);
+            }
           }
-          if (hf == 0) rm0 = mx; else rm1 = mx;
-        }
-        if (KS == 1) {
-          rm0 = fmaxf(rm0, rm1);
-          rm1 = rm0;
+          if (KS == 1) {
+            rm0 = fmaxf(rm0, rm1);
+            rm1 = rm0;
+          }
         }
 
         // Block classes of the (query, key) sub-blocks of this tile.
-        int cls[2][2];
+        int cls[2][2] = {{0, 0}, {0, 0}};
+        if (simple) {
+          cls[0][0] = diag_tile ? 2 : 1;
+        } else {
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+          for (int q = 0; q < 2; ++q)
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
-            cls[q][k] = (q < QS && k < KS)
-                            ? block_class(iq_base + q, (J * TILE) / p.Bk + k, p.Bq, p.Bk, len)
-                            : 0;
+            for (int k = 0; k < 2; ++k)
+              if (q < QS && k < KS)
+                cls[q][k] = block_class(iq_base + q, (J * TILE) / p.Bk + k, p.Bq, p.Bk, len);
+        }
+
+        // ---- warp-level reduction for the gate (threshold / calibration)
+        // or the first vote (lambda); one barrier per tile also settles
+        // whether every thread of the warpgroup is still running.
+        const bool lambda_mode = GATING && !CALIB && p.mode == 1;
+        bool want0 = false;
+        if (CALIB || (GATING && !lambda_mode)) {
+          const float w0 = warp_max_f32(rvalid ? rm0 : -CUDART_INF_F);
+          const float w1 = (KS == 1) ? w0 : warp_max_f32(rvalid ? rm1 : -CUDART_INF_F);
+          if (lane == 0) {
+            c->red[s][tb][wq][0] = w0;
+            c->red[s][tb][wq][1] = w1;
+          }
+        } else if (lambda_mode) {
+          want0 = rvalid && cls[myqs][0] == 1 && ((rm0 - m_true) * p.sigma >= p.log_lambda);
+          const unsigned any = __ballot_sync(0xffffffffu, want0);
+          if (lane == 0) c->red[s][tb][wq][0] = any ? 1.f : 0.f;
+        }
+        if (!(ok = bar_red_and(bar_id, 128, okl))) break;
 
         if constexpr (CALIB) {
           // Calibration: record sigma * s_max for candidate blocks.
-          const float v0 = rvalid ? rm0 : -CUDART_INF_F;
-          const float v1 = rvalid ? rm1 : -CUDART_INF_F;
-          const float w0 = warp_max(v0), w1 = warp_max(v1);
-          const int rb = nsync & 1;
-          if (lane == 0) {
-            c->red[s][rb][wq][0] = w0;
-            c->red[s][rb][wq][1] = w1;
-            mbar_arrive(&c->wg[s][rb]);
-          }
-          if (!(ok = wait_bar(&c->wg[s][rb], (nsync >> 1) & 1, abort, p.err, ERR_WAIT_WG)))
-            break;
-          ++nsync;
           if (row == 0) {
             for (int q = 0; q < QS; ++q)
               for (int k = 0; k < KS; ++k) {
                 if (cls[q][k] != 1) continue;
                 float mx = -CUDART_INF_F;
                 for (int w = 0; w < 4; ++w)
-                  if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][rb][w][k]);
+                  if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][tb][w][k]);
                 const long long idx =
                     ((long long)h * p.cal_nq + iq_base + q) * p.cal_nk + (J * TILE) / p.Bk + k;
                 p.blockmax[idx] = mx * p.sigma;
@@ -500,19 +537,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 #pragma unroll
             for (int k = 0; k < 2; ++k) keep[q][k] = cls[q][k] != 0;
           if constexpr (GATING) {
-            if (p.mode == 0) {
-              const float v0 = rvalid ? rm0 : -CUDART_INF_F;
-              const float v1 = rvalid ? rm1 : -CUDART_INF_F;
-              const float w0 = warp_max(v0), w1 = warp_max(v1);
-              const int rb = nsync & 1;
-              if (lane == 0) {
-                c->red[s][rb][wq][0] = w0;
-                c->red[s][rb][wq][1] = w1;
-                mbar_arrive(&c->wg[s][rb]);
-              }
-              if (!(ok = wait_bar(&c->wg[s][rb], (nsync >> 1) & 1, abort, p.err, ERR_WAIT_WG)))
-                break;
-              ++nsync;
+            if (!lambda_mode) {
 #pragma unroll
               for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -521,44 +546,42 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                   float mx = -CUDART_INF_F;
 #pragma unroll
                   for (int w = 0; w < 4; ++w)
-                    if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][rb][w][k]);
+                    if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][tb][w][k]);
                   keep[q][k] = (mx * p.sigma) >= thr[q];
                 }
             } else {
-              // lambda: sub-blocks in ascending key order; the running max of
-              // a row moves only with the blocks it keeps.
+              // lambda: sub-blocks in ascending key order; a row's running
+              // max moves only with the blocks it keeps.
 #pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                if (k >= KS) break;
-                const float rmk = (k == 0) ? rm0 : rm1;
-                bool need_vote = false;
+              for (int q = 0; q < 2; ++q) {
+                if (cls[q][0] != 1) continue;
+                bool kp = false;
 #pragma unroll
-                for (int q = 0; q < 2; ++q) need_vote |= (cls[q][k] == 1);
+                for (int w = 0; w < 4; ++w)
+                  if (QS == 1 || (w >> 1) == q) kp |= (c->red[s][tb][w][0] != 0.f);
+                keep[q][0] = kp;
+              }
+              if (keep[myqs][0]) m_true = fmaxf(m_true, rm0);
+              if (KS == 2) {
+                bool need_vote = (cls[0][1] == 1) || (cls[1][1] == 1);
                 if (need_vote) {
-                  const bool want =
-                      rvalid && cls[myqs][k] == 1 && ((rmk - m_true) * p.sigma >= p.log_lambda);
-                  const unsigned any = __ballot_sync(0xffffffffu, want);
-                  const int rb = nsync & 1;
-                  if (lane == 0) {
-                    c->red[s][rb][wq][k] = any ? 1.f : 0.f;
-                    mbar_arrive(&c->wg[s][rb]);
-                  }
-                  if (!(ok = wait_bar(&c->wg[s][rb], (nsync >> 1) & 1, abort, p.err, ERR_WAIT_WG)))
-                    break;
-                  ++nsync;
+                  const bool want1 =
+                      rvalid && cls[myqs][1] == 1 && ((rm1 - m_true) * p.sigma >= p.log_lambda);
+                  const unsigned any = __ballot_sync(0xffffffffu, want1);
+                  if (lane == 0) c->red[s][tb][wq][1] = any ? 1.f : 0.f;
+                  named_bar_sync(bar_id, 128);
 #pragma unroll
                   for (int q = 0; q < 2; ++q) {
-                    if (cls[q][k] != 1) continue;
+                    if (cls[q][1] != 1) continue;
                     bool kp = false;
 #pragma unroll
                     for (int w = 0; w < 4; ++w)
-                      if (QS == 1 || (w >> 1) == q) kp |= (c->red[s][rb][w][k] != 0.f);
-                    keep[q][k] = kp;
+                      if (QS == 1 || (w >> 1) == q) kp |= (c->red[s][tb][w][1] != 0.f);
+                    keep[q][1] = kp;
                   }
                 }
-                if (keep[myqs][k]) m_true = fmaxf(m_true, rmk);
+                if (keep[myqs][1]) m_true = fmaxf(m_true, rm1);
               }
-              if (!ok) break;
             }
           }
           uint32_t decbits = 0;
@@ -604,15 +627,15 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             if (k0) rmk = fmaxf(rmk, rm0);
             if (k1) rmk = fmaxf(rmk, rm1);
             const float m_new = fmaxf(m_used, rmk);
-            const bool resc = (m_new - m_used) * p.sigma_log2 > RESCALE_LOG2;
+            const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
             float alpha = 1.f;
             if (resc) {
-              alpha = ex2_approx((m_used - m_new) * p.sigma_log2);
+              alpha = ex2_approx((m_used - m_new) * sc);
               m_used = m_new;
               l *= alpha;
             }
             if (o_init && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
+#pragma unroll 1
               for (int q = 0; q < D / 32; ++q) {
                 uint32_t orr[32];
                 tmem_ld32(tO + q * 32, orr);
@@ -626,9 +649,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             // Pass 2: P = exp2(sigma*log2e*(S - m)) for the kept, visible
             // entries, packed as bf16 pairs into the first 64 columns of the
             // S region (half hf of S -> P columns [32 hf, 32 hf + 32); those
-            // S columns were already read).
-            const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * p.sigma_log2;
-            float lsum = 0.f;
+            // S columns have already been read).
+            const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * sc;
+            const uint64_t sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
+            uint64_t lsum2 = f2_pack(0.f, 0.f);
+            const bool fast = !diag_tile && k0 && k1;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               const bool kk = (hf == 0) ? k0 : k1;
@@ -637,21 +662,37 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
               tmem_ld32(tS + hf * 64 + 32, sr[1]);
               tmem_wait_ld();
               uint32_t pk[32];
+              if (fast) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int cc = hf * 64 + 2 * e;
-                const bool vis0 = kk && !(diag_tile && cc > row);
-                const bool vis1 = kk && !(diag_tile && cc + 1 > row);
-                const float x0 = __uint_as_float(sr[(2 * e) >> 5][(2 * e) & 31]);
-                const float x1 = __uint_as_float(sr[(2 * e + 1) >> 5][(2 * e + 1) & 31]);
-                const float p0 = vis0 ? ex2_approx(fmaf(x0, p.sigma_log2, -mb)) : 0.f;
-                const float p1 = vis1 ? ex2_approx(fmaf(x1, p.sigma_log2, -mb)) : 0.f;
-                lsum += p0 + p1;
-                pk[e] = pack_bf16x2(p0, p1);
+                for (int e = 0; e < 32; ++e) {
+                  const uint64_t x2 = f2_pack(__uint_as_float(sr[e >> 4][(2 * e) & 31]),
+                                              __uint_as_float(sr[e >> 4][(2 * e + 1) & 31]));
+                  float y0, y1;
+                  f2_unpack(f2_fma(x2, sc2, nmb2), y0, y1);
+                  const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+                  const uint64_t pp = f2_pack(p0, p1);
+                  lsum2 = f2_add(lsum2, pp);
+                  pk[e] = pack_bf16x2(p0, p1);
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  const int cc = hf * 64 + 2 * e;
+                  const bool vis0 = kk && !(diag_tile && cc > row);
+                  const bool vis1 = kk && !(diag_tile && cc + 1 > row);
+                  const float x0 = __uint_as_float(sr[e >> 4][(2 * e) & 31]);
+                  const float x1 = __uint_as_float(sr[e >> 4][(2 * e + 1) & 31]);
+                  const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
+                  const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
+                  lsum2 = f2_add(lsum2, f2_pack(p0, p1));
+                  pk[e] = pack_bf16x2(p0, p1);
+                }
               }
               tmem_st32(tS + hf * 32, pk);
             }
-            l += lsum;
+            float ls0, ls1;
+            f2_unpack(lsum2, ls0, ls1);
+            l += ls0 + ls1;
             tmem_wait_st();
             o_init = true;
           }
@@ -667,11 +708,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
           p.bitmap[bm_row + bm_idx] = bm_word;
           for (int w = bm_idx + 1; w < p.words; ++w) p.bitmap[bm_row + w] = 0u;
         }
-        if (!(ok = wait_bar(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL))) break;
+        const bool okl = wait_bar(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL);
+        if (!(ok = bar_red_and(bar_id, 128, okl))) break;
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        __nv_bfloat16* orow =
-            p.o + (long long)si.w * p.o_sb + (long long)h * p.o_sh + (long long)(si.x + qpos) * p.o_st;
+        __nv_bfloat16* orow = p.o + (long long)si.w * p.o_sb + (long long)h * p.o_sh +
+                              (long long)(si.x + qpos) * p.o_st;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
           uint32_t orr[32];
@@ -703,7 +745,6 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       atomicAdd(&p.counts[2], cnt_diag);
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

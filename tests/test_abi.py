@@ -1,0 +1,76 @@
+"""The C-ABI library loads and exports every function include/*.h declares,
+and the binding's ctypes signatures cover the same set.  No GPU compute."""
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(bsfa_[a-z_0-9]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from block_sparse_gated_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_boundary():
+    d = _declared()
+    for name in ("bsfa_prefill_fwd", "bsfa_calibrate", "bsfa_prefill_workspace_size",
+                 "bsfa_calibrate_workspace_size", "bsfa_device_error", "bsfa_status_string"):
+        assert name in d
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    out = subprocess.run(["nm", "-D", "--defined-only", libpath], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = _declared() - exported
+    assert not missing, f"declared but not exported: {sorted(missing)}"
+
+
+def test_ctypes_binding_loads_every_symbol(libpath):
+    from block_sparse_gated_gb300 import _native
+    L = _native.lib()
+    bound = {name for name, _, _ in _native.SIGNATURES}
+    assert bound == _declared()
+    for name in bound:
+        assert getattr(L, name) is not None
+
+
+def test_host_side_validation_without_gpu(libpath):
+    """Calls that fail host validation return before touching the device."""
+    import ctypes
+    from block_sparse_gated_gb300 import _native
+    L = _native.lib()
+    assert L.bsfa_version() > 0
+    assert L.bsfa_status_string(0) == b"ok"
+    p = _native.FwdParams()
+    p.batch, p.num_heads_q, p.num_heads_kv, p.seqlen, p.head_dim = 1, 4, 3, 128, 128
+    p.block_q = p.block_k = 128
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # Hq % Hkv != 0
+    p.num_heads_kv, p.head_dim = 2, 96
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unsupported head_dim
+    p.head_dim, p.block_k = 128, 96
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unsupported block size
+    p.block_k = 128
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # null tensors
+    p.batch = 0
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 0  # empty batch is a no-op
+    p.batch = 2
+    assert L.bsfa_prefill_workspace_size(ctypes.byref(p)) > 0
+    w = ctypes.c_int(0)
+    assert L.bsfa_bitmap_words_per_row(ctypes.byref(p), ctypes.byref(w)) == 0 and w.value == 1

@@ -46,6 +46,7 @@ SIGNATURES = [
         ctypes.POINTER(c_int64), ctypes.POINTER(c_int64), c_int, c_int, c_float,
         ctypes.POINTER(c_int), c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     ("bsfa_device_error", c_int, [c_void_p, ctypes.POINTER(ctypes.c_uint)]),
+    ("bsfa_prefill_fwd_noalloc", c_int, [ctypes.POINTER(FwdParams), c_void_p]),
 ]
 
 _lib = None

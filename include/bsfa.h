@@ -140,6 +140,38 @@ bsfa_status bsfa_bitmap_words_per_row(const bsfa_fwd_params* p, int* words_per_r
 bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream);
 
 /*
+ * bsfa_prefill_fwd_noalloc -- the same gated prefill for callers that cannot
+ * allocate device memory at call time.  The paper has no counterpart to this
+ * entry point; it exists for the calling environment, not for the method.
+ *
+ * Who needs it: callers whose device memory is planned once, up front, and
+ * who may not call cudaMalloc (or any allocator) while attention runs --
+ * real-time serving loops with a fixed memory plan, plugins hosted by a
+ * framework that owns the allocator, embedded runtimes with a static memory
+ * map.  bsfa_prefill_fwd asks for a caller-provided workspace; this entry
+ * point takes none.
+ *
+ * Behaviour: identical to bsfa_prefill_fwd, except that p->workspace and
+ * p->workspace_bytes are ignored.  The scratch (sequence table and tile
+ * schedule) lives in a fixed 256 KiB array of device memory that the library
+ * sets aside on every GPU that loads it, for the life of the process.
+ *   - Limit: the call's bsfa_prefill_workspace_size(p) must not exceed
+ *     262144 bytes (for example 32 sequences of 32K tokens need about 66 KiB;
+ *     one sequence may have up to 16384 query tiles of 128 rows).  A larger
+ *     request returns BSFA_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the array's device address and
+ *     caches it; make that first call before any stream capture begins.
+ *   - All calls on a device share the one array, which keeps the previous
+ *     call's contents.  Each call rewrites every scratch byte it later reads,
+ *     so nothing has to start at zero.  Calls that may overlap on the GPU
+ *     (different streams with no ordering between them) race on the array:
+ *     order them on one stream, or use bsfa_prefill_fwd with separate
+ *     workspaces.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+bsfa_status bsfa_prefill_fwd_noalloc(const bsfa_fwd_params* p, bsfa_stream_t stream);
+
+/*
  * Offline threshold calibration for one layer and a set of budgets.
  *   q_samples / k_samples: HOST arrays of n_samples DEVICE pointers to bf16
  *     tensors of one sample each, layout [H, L, d] addressed by the strides

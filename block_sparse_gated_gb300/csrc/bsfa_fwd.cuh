@@ -78,6 +78,8 @@ struct Ctrl {
   uint32_t tmem_base;
   uint32_t dec[NQ][2];
   float red[NQ][2][4][2];
+  alignas(16) uint32_t vote[NQ][2][4];   // per warp: bit k = some row wants key half k
+  alignas(16) uint32_t vote2[NQ][2][4];  // lambda, second key half
   int abort;
 };
 
@@ -114,6 +116,24 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
       }
     }
   }
+}
+
+// wait_bar executed by every lane of a warp, with the lanes agreeing on the
+// outcome (a phase seen complete by one lane is complete for all of them;
+// only a lane that timed out can disagree, and then the whole warp stops).
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         unsigned* err, unsigned site) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, err, site));
+}
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // Bounded wait used only on the abort path: ignores the abort flag so that
@@ -155,6 +175,27 @@ __device__ __forceinline__ int block_class(int i, int j, int Bq, int Bk, int L) 
   if ((j + 1) * Bk <= first_row) return 1;
   if (first_key <= last_row) return 2;
   return 0;
+}
+
+// S = Q K^T for one slot: D/16 K-steps of M=128, N=128, K=16.  Operand
+// halves (64 columns, 16 KB each) sit TILE*128 bytes apart.
+template <int D, int NQ>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (((kk >> 2) * (TILE * 128)) + (kk & 3) * 32) >> 4;
+    umma_ss(d_tmem, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V for one slot: 8 K-steps of 16 keys; P (bf16 pairs) in TMEM
+// columns [8 kk, 8 kk + 8) of the S region, V MN-major (16 keys = 2048 B).
+template <int D, int NQ>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv,
+                                         uint32_t idesc, uint32_t acc) {
+#pragma unroll
+  for (int kk = 0; kk < TILE / 16; ++kk)
+    umma_ts(d_tmem, p_tmem + kk * 8, dv + ((kk * 2048) >> 4), idesc, (kk > 0 || acc) ? 1u : 0u);
 }
 
 template <int D, int NQ, bool GATING, bool CALIB>
@@ -218,190 +259,215 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
   const int HP = p.Hkv * p.pairs;
   const int total_units = (*p.ntiles_total) * HP;
 
+  // Register split for two slots (launched at 168 per thread, 384 threads):
+  // warpgroup 0 (copies, MMA issue) gives up to 56, the two softmax
+  // warpgroups rise to 224: 128*56 + 256*224 = 384*168.  Each role sets its
+  // own limit at the top of its branch.
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
-      int last_q = -1;  // index of the last unit whose Q load was issued
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
-        const int2 t = p.tiles[u / HP];
-        const int hp = u % HP, kvh = hp / p.pairs, pr = hp % p.pairs;
-        const int4 si = p.seqinfo[t.x];
-        const int I = t.y, nkt = I + 1;
-        const int row0 = si.x + I * TILE;
-        if (!(ok = wait_bar(&c->q_empty, (uc & 1) ^ 1, abort, p.err, ERR_WAIT_Q_EMPTY))) break;
+    if constexpr (NQ == 2) setmaxnreg_dec<56>();
+    // The whole warp runs the loop and the waits (so every value it uses is
+    // warp-uniform); one elected lane issues each copy.
+    uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
+    int last_q = -1;  // index of the last unit whose Q load was issued
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+      const int2 t = p.tiles[u / HP];
+      const int hp = u % HP, kvh = hp / p.pairs, pr = hp % p.pairs;
+      const int4 si = p.seqinfo[t.x];
+      const int I = t.y, nkt = I + 1;
+      const int row0 = si.x + I * TILE;
+      if (!(ok = wait_all(&c->q_empty, (uc & 1) ^ 1, abort, p.err, ERR_WAIT_Q_EMPTY))) break;
+      if (elect_one()) {
         for (int s = 0; s < NQ; ++s) {
           const int h = kvh * p.group + pr * NQ + s;
           mbar_arrive_expect_tx(&c->q_full[s], TB);
           for (int hf = 0; hf < NHALF; ++hf)
             tma_load_4d(sQ + s * TB + hf * HALF, &tmQ, &c->q_full[s], hf * 64, row0, h, si.w);
         }
-        last_q = static_cast<int>(uc);
-        auto issue_k = [&](int J) -> bool {
+      }
+      __syncwarp();
+      last_q = static_cast<int>(uc);
+      for (int J = -1; J < nkt; ++J) {
+        // K for tile J + 1 (tile 0 before the loop proper), then V for tile J.
+        if (J + 1 < nkt) {
           const uint32_t st = kc % KST;
-          if (!wait_bar(&c->k_empty[st], ((kc / KST) & 1) ^ 1, abort, p.err, ERR_WAIT_K_EMPTY))
-            return false;
-          mbar_arrive_expect_tx(&c->k_full[st], TB);
-          for (int hf = 0; hf < NHALF; ++hf)
-            tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64,
-                        si.x + J * TILE, kvh, si.w);
+          if (!(ok = wait_all(&c->k_empty[st], ((kc / KST) & 1) ^ 1, abort, p.err,
+                              ERR_WAIT_K_EMPTY)))
+            break;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&c->k_full[st], TB);
+            for (int hf = 0; hf < NHALF; ++hf)
+              tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64,
+                          si.x + (J + 1) * TILE, kvh, si.w);
+          }
+          __syncwarp();
           ++kc;
-          return true;
-        };
-        if (!(ok = issue_k(0))) break;
-        for (int J = 0; J < nkt; ++J, ++tc) {
-          if (J + 1 < nkt && !(ok = issue_k(J + 1))) break;
-          if constexpr (!CALIB) {
-            bool need = true;
-            if constexpr (GATING) {
-              need = false;
-              for (int s = 0; s < NQ; ++s) {
-                if (!(ok = wait_bar(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
-                                    ERR_WAIT_DEC)))
-                  break;
-                if (c->dec[s][tc & 1] != 0u) {
-                  need = true;
-                  break;
-                }
-              }
-              if (!ok) break;
-            }
-            if (need) {
-              const uint32_t st = vc % VST;
-              if (!(ok = wait_bar(&c->v_empty[st], ((vc / VST) & 1) ^ 1, abort, p.err,
-                                  ERR_WAIT_V_EMPTY)))
+        }
+        if (J < 0) continue;
+        if constexpr (!CALIB) {
+          bool need = true;
+          if constexpr (GATING) {
+            need = false;
+            for (int s = 0; s < NQ; ++s) {
+              if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
+                                  ERR_WAIT_DEC)))
                 break;
+              if (c->dec[s][tc & 1] != 0u) {
+                need = true;
+                break;
+              }
+            }
+            if (!ok) break;
+          }
+          if (need) {
+            const uint32_t st = vc % VST;
+            if (!(ok = wait_all(&c->v_empty[st], ((vc / VST) & 1) ^ 1, abort, p.err,
+                                ERR_WAIT_V_EMPTY)))
+              break;
+            if (elect_one()) {
               mbar_arrive_expect_tx(&c->v_full[st], TB);
               for (int hf = 0; hf < NHALF; ++hf)
                 tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64,
                             si.x + J * TILE, kvh, si.w);
-              ++vc;
             }
+            __syncwarp();
+            ++vc;
           }
         }
+        ++tc;
       }
-      if (!ok) {
-        // Let every copy already issued land before the CTA can exit.
-        for (int s = 0; s < NQ && last_q >= 0; ++s) drain_wait(&c->q_full[s], last_q & 1);
-        for (uint32_t i = 0; i < KST && i < kc; ++i) {
-          const uint32_t f = kc - 1 - i;
-          drain_wait(&c->k_full[f % KST], (f / KST) & 1);
-        }
-        for (uint32_t i = 0; i < VST && i < vc; ++i) {
-          const uint32_t f = vc - 1 - i;
-          drain_wait(&c->v_full[f % VST], (f / VST) & 1);
-        }
+    }
+    if (!ok) {
+      // Let every copy already issued land before the CTA can exit.
+      for (int s = 0; s < NQ && last_q >= 0; ++s) drain_wait(&c->q_full[s], last_q & 1);
+      for (uint32_t i = 0; i < KST && i < kc; ++i) {
+        const uint32_t f = kc - 1 - i;
+        drain_wait(&c->k_full[f % KST], (f / KST) & 1);
+      }
+      for (uint32_t i = 0; i < VST && i < vc; ++i) {
+        const uint32_t f = vc - 1 - i;
+        drain_wait(&c->v_full[f % VST], (f / VST) & 1);
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
-      uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
-      bool ok = true;
-      auto issue_qk = [&](int s, uint32_t st) {
-        const uint32_t d_tmem = tmem + s * 128;
-        const uint32_t qa = smem_u32(sQ + s * TB), ka = smem_u32(sK + st * TB);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-          umma_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                  IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int s, uint32_t st, uint32_t acc) {
-        const uint32_t d_tmem = tmem + NQ * 128 + s * D;
-        const uint32_t va = smem_u32(sV + st * TB);
-#pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk)
-          umma_ts(d_tmem, tmem + s * 128 + kk * 8, smem_desc_sw128(va + kk * 2048, HALF, 1024),
-                  IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
-      };
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
-        const int2 t = p.tiles[u / HP];
-        const int nkt = t.y + 1;
-        for (int s = 0; s < NQ && ok; ++s)
-          ok = wait_bar(&c->q_full[s], uc & 1, abort, p.err, ERR_WAIT_Q_FULL);
-        if (!ok) break;
-        {
-          const uint32_t st = kc % KST;
-          if (!(ok = wait_bar(&c->k_full[st], (kc / KST) & 1, abort, p.err, ERR_WAIT_K_FULL))) break;
-          tc_fence_after();
+    if constexpr (NQ == 2) setmaxnreg_dec<56>();
+    // The whole warp runs the loop and the waits; one elected lane (always
+    // the same lane: all 32 are active) issues every MMA and commit, so each
+    // commit tracks that lane's earlier MMAs.
+    constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
+    uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
+    bool ok = true;
+    // Descriptors: one 64-bit base per operand buffer; a K-step adds its
+    // byte offset >> 4 to the start-address field (bits 0-13; every
+    // shared-memory address here is < 2^18, so the field never carries).
+    const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t dV = smem_desc_sw128(smem_u32(sV), HALF, 1024);
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+      const int2 t = p.tiles[u / HP];
+      const int nkt = t.y + 1;
+      for (int s = 0; s < NQ && ok; ++s)
+        ok = wait_all(&c->q_full[s], uc & 1, abort, p.err, ERR_WAIT_Q_FULL);
+      if (!ok) break;
+      {
+        const uint32_t st = kc % KST;
+        if (!(ok = wait_all(&c->k_full[st], (kc / KST) & 1, abort, p.err, ERR_WAIT_K_FULL))) break;
+        if (elect_one()) {
           for (int s = 0; s < NQ; ++s) {
-            issue_qk(s, st);
+            issue_qk<D, NQ>(tmem + s * 128, dQ + ((s * TB) >> 4), dK + ((st * TB) >> 4), IDESC_QK);
             umma_commit(&c->s_full[s]);
           }
           umma_commit(&c->k_empty[st]);
-          ++kc;
           if (nkt == 1) umma_commit(&c->q_empty);
         }
-        bool first[NQ];
-        for (int s = 0; s < NQ; ++s) first[s] = true;
-        for (int J = 0; J < nkt && ok; ++J, ++tc) {
-          const int tb = tc & 1;
-          const uint32_t vst = vc % VST;
-          const uint32_t kst = kc % KST;
-          bool vready = false, any = false;
-          for (int s = 0; s < NQ; ++s) {
-            if (!(ok = wait_bar(&c->p_full[s], tc & 1, abort, p.err, ERR_WAIT_P_FULL))) break;
-            tc_fence_after();
-            if constexpr (!CALIB) {
-              const uint32_t dec = GATING ? c->dec[s][tb] : 1u;
-              if (dec != 0u) {
-                any = true;
-                if (!vready) {
-                  if (!(ok = wait_bar(&c->v_full[vst], (vc / VST) & 1, abort, p.err,
-                                      ERR_WAIT_V_FULL)))
-                    break;
-                  tc_fence_after();
-                  vready = true;
-                }
-                uint32_t acc = 1u;
-                if (first[s]) {
-                  if (!(ok = wait_bar(&c->o_empty[s], (uc & 1) ^ 1, abort, p.err,
-                                      ERR_WAIT_O_EMPTY)))
-                    break;
-                  tc_fence_after();
-                  acc = 0u;
-                  first[s] = false;
-                }
-                issue_pv(s, vst, acc);
+        __syncwarp();
+        ++kc;
+      }
+      uint32_t first_mask = (1u << NQ) - 1u;  // slots whose O has not been written yet
+      for (int J = 0; J < nkt && ok; ++J, ++tc) {
+        const int tb = tc & 1;
+        const uint32_t vst = vc % VST;
+        const uint32_t kst = kc % KST;
+        bool vready = false, any = false;
+        for (int s = 0; s < NQ; ++s) {
+          if (!(ok = wait_all(&c->p_full[s], tc & 1, abort, p.err, ERR_WAIT_P_FULL))) break;
+          tc_fence_after();
+          bool do_pv = false;
+          uint32_t acc = 1u;
+          if constexpr (!CALIB) {
+            const uint32_t dec = GATING ? c->dec[s][tb] : 1u;
+            if (dec != 0u) {
+              any = true;
+              do_pv = true;
+              if (!vready) {
+                // V arrives by TMA into shared memory: the mbarrier completion
+                // orders it before the MMA (no TMEM hand-off, no tcgen05 fence).
+                if (!(ok = wait_all(&c->v_full[vst], (vc / VST) & 1, abort, p.err,
+                                    ERR_WAIT_V_FULL)))
+                  break;
+                vready = true;
               }
-            }
-            if (J + 1 < nkt) {
-              if (s == 0) {
-                if (!(ok = wait_bar(&c->k_full[kst], (kc / KST) & 1, abort, p.err,
-                                    ERR_WAIT_K_FULL)))
+              if (first_mask & (1u << s)) {
+                if (!(ok = wait_all(&c->o_empty[s], (uc & 1) ^ 1, abort, p.err,
+                                    ERR_WAIT_O_EMPTY)))
                   break;
                 tc_fence_after();
+                acc = 0u;
+                first_mask &= ~(1u << s);
               }
-              issue_qk(s, kst);
+            }
+          }
+          const bool do_qk = J + 1 < nkt;
+          // P.V for this tile first: it does not need the next K tile.
+          if (do_pv && elect_one())
+            issue_pv<D, NQ>(tmem + NQ * 128 + s * D, tmem + s * 128, dV + ((vst * TB) >> 4),
+                            IDESC_PV, acc);
+          __syncwarp();
+          if (do_qk && s == 0) {
+            if (!(ok = wait_all(&c->k_full[kst], (kc / KST) & 1, abort, p.err, ERR_WAIT_K_FULL)))
+              break;
+          }
+          if (elect_one()) {
+            if (do_qk) {
+              issue_qk<D, NQ>(tmem + s * 128, dQ + ((s * TB) >> 4), dK + ((kst * TB) >> 4),
+                              IDESC_QK);
               umma_commit(&c->s_full[s]);
               if (s == NQ - 1) {
                 umma_commit(&c->k_empty[kst]);
-                ++kc;
                 if (J + 1 == nkt - 1) umma_commit(&c->q_empty);
               }
             }
           }
-          if (!ok) break;
-          if (!CALIB && any) {
-            umma_commit(&c->v_empty[vst]);
-            ++vc;
-          }
+          __syncwarp();
+          if (do_qk && s == NQ - 1) ++kc;
         }
         if (!ok) break;
-        if constexpr (!CALIB)
-          for (int s = 0; s < NQ; ++s) umma_commit(&c->o_full[s]);
+        if (!CALIB && any) {
+          if (elect_one()) umma_commit(&c->v_empty[vst]);
+          __syncwarp();
+          ++vc;
+        }
       }
-      // Drain: every issued MMA completes before TMEM can be released.
-      umma_commit(&c->drain);
-      drain_wait(&c->drain, 0);
+      if (!ok) break;
+      if constexpr (!CALIB) {
+        if (elect_one())
+          for (int s = 0; s < NQ; ++s) umma_commit(&c->o_full[s]);
+        __syncwarp();
+      }
     }
-  } else if (warp >= 4) {
+    // Drain: every issued MMA completes before TMEM can be released.
+    if (elect_one()) umma_commit(&c->drain);
+    __syncwarp();
+    drain_wait(&c->drain, 0);
+  } else if (warp < 4) {
+    if constexpr (NQ == 2) setmaxnreg_dec<56>();
+  } else {
     // -------------------------------------------------------------- softmax
+    if constexpr (NQ == 2) setmaxnreg_inc<224>();
     const int s = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
@@ -430,8 +496,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       const int my_i = iq_base + myqs;
       float thr[2] = {0.f, 0.f};
       if (GATING && !CALIB && p.mode == 0) {
-        for (int q = 0; q < QS; ++q)
-          thr[q] = p.thr[(long long)h * p.nT + min(iq_base + q, p.nT - 1)];
+        thr[0] = p.thr[(long long)h * p.nT + min(iq_base, p.nT - 1)];
+        if (QS == 2) thr[1] = p.thr[(long long)h * p.nT + min(iq_base + 1, p.nT - 1)];
       }
       float m_used = -CUDART_INF_F, m_true = -CUDART_INF_F, l = 0.f;
       bool o_init = false;
@@ -448,8 +514,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 
         // ---- pass 1: row maxima of the two 64-key halves of S
         float rm0 = -CUDART_INF_F, rm1 = -CUDART_INF_F;
+        uint32_t sr[4][32];
         if (okl) {
-          uint32_t sr[4][32];
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
           tmem_wait_ld();
@@ -493,22 +559,33 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                 cls[q][k] = block_class(iq_base + q, (J * TILE) / p.Bk + k, p.Bq, p.Bk, len);
         }
 
-        // ---- warp-level reduction for the gate (threshold / calibration)
-        // or the first vote (lambda); one barrier per tile also settles
-        // whether every thread of the warpgroup is still running.
+        // ---- gate votes.  Threshold: row r wants key half k when
+        // sigma * rowmax_r(k) >= T.  The tile maximum clears T exactly when
+        // some row's maximum does (scaling by sigma > 0 is monotone in fp32),
+        // so the OR of the row votes equals comparing s_max(i,j) with T.
+        // Lambda: row r wants the first sub-block when
+        // sigma * (rowmax_r - m_r) >= ln(lambda).  One barrier per tile also
+        // settles whether every thread of the warpgroup is still running.
         const bool lambda_mode = GATING && !CALIB && p.mode == 1;
-        bool want0 = false;
-        if (CALIB || (GATING && !lambda_mode)) {
+        if constexpr (CALIB) {
           const float w0 = warp_max_f32(rvalid ? rm0 : -CUDART_INF_F);
           const float w1 = (KS == 1) ? w0 : warp_max_f32(rvalid ? rm1 : -CUDART_INF_F);
           if (lane == 0) {
             c->red[s][tb][wq][0] = w0;
             c->red[s][tb][wq][1] = w1;
           }
-        } else if (lambda_mode) {
-          want0 = rvalid && cls[myqs][0] == 1 && ((rm0 - m_true) * p.sigma >= p.log_lambda);
-          const unsigned any = __ballot_sync(0xffffffffu, want0);
-          if (lane == 0) c->red[s][tb][wq][0] = any ? 1.f : 0.f;
+        } else if constexpr (GATING) {
+          bool w0, w1 = false;
+          if (!lambda_mode) {
+            const float tq = (myqs ? thr[1] : thr[0]);
+            w0 = rvalid && rm0 * p.sigma >= tq;
+            w1 = rvalid && rm1 * p.sigma >= tq;
+          } else {
+            w0 = rvalid && (myqs ? cls[1][0] : cls[0][0]) == 1 && ((rm0 - m_true) * p.sigma >= p.log_lambda);
+          }
+          const uint32_t bits = (__any_sync(0xffffffffu, w0) ? 1u : 0u) |
+                                ((KS == 2 && __any_sync(0xffffffffu, w1)) ? 2u : 0u);
+          if (lane == 0) c->vote[s][tb][wq] = bits;
         }
         if (!(ok = bar_red_and(bar_id, 128, okl))) break;
 
@@ -537,50 +614,34 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 #pragma unroll
             for (int k = 0; k < 2; ++k) keep[q][k] = cls[q][k] != 0;
           if constexpr (GATING) {
-            if (!lambda_mode) {
+            // OR the warp votes of each query half (warps 0-1 hold rows 0-63).
+            const uint4 vv = *reinterpret_cast<const uint4*>(&c->vote[s][tb][0]);
+            uint32_t vq0 = vv.x | vv.y, vq1 = vv.z | vv.w;
+            if (QS == 1) vq0 = vq1 = vq0 | vq1;
 #pragma unroll
-              for (int q = 0; q < 2; ++q)
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                  if (cls[q][k] != 1) continue;
-                  float mx = -CUDART_INF_F;
-#pragma unroll
-                  for (int w = 0; w < 4; ++w)
-                    if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][tb][w][k]);
-                  keep[q][k] = (mx * p.sigma) >= thr[q];
-                }
-            } else {
-              // lambda: sub-blocks in ascending key order; a row's running
-              // max moves only with the blocks it keeps.
-#pragma unroll
-              for (int q = 0; q < 2; ++q) {
-                if (cls[q][0] != 1) continue;
-                bool kp = false;
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                  if (QS == 1 || (w >> 1) == q) kp |= (c->red[s][tb][w][0] != 0.f);
-                keep[q][0] = kp;
-              }
-              if (keep[myqs][0]) m_true = fmaxf(m_true, rm0);
+            for (int k = 0; k < 2; ++k) {
+              if (cls[0][k] == 1) keep[0][k] = (vq0 >> k) & 1u;
+              if (cls[1][k] == 1) keep[1][k] = (vq1 >> k) & 1u;
+            }
+            if (lambda_mode) {
+              // Sub-blocks in ascending key order; a row's running max moves
+              // only with the blocks it keeps, so the second key half is voted
+              // on after the first half's decision.
+              if ((myqs ? keep[1][0] : keep[0][0])) m_true = fmaxf(m_true, rm0);
               if (KS == 2) {
-                bool need_vote = (cls[0][1] == 1) || (cls[1][1] == 1);
-                if (need_vote) {
-                  const bool want1 =
-                      rvalid && cls[myqs][1] == 1 && ((rm1 - m_true) * p.sigma >= p.log_lambda);
-                  const unsigned any = __ballot_sync(0xffffffffu, want1);
-                  if (lane == 0) c->red[s][tb][wq][1] = any ? 1.f : 0.f;
+                if (cls[0][1] == 1 || cls[1][1] == 1) {
+                  const bool w1 =
+                      rvalid && (myqs ? cls[1][1] : cls[0][1]) == 1 && ((rm1 - m_true) * p.sigma >= p.log_lambda);
+                  const uint32_t b1 = __any_sync(0xffffffffu, w1) ? 1u : 0u;
+                  if (lane == 0) c->vote2[s][tb][wq] = b1;
                   named_bar_sync(bar_id, 128);
-#pragma unroll
-                  for (int q = 0; q < 2; ++q) {
-                    if (cls[q][1] != 1) continue;
-                    bool kp = false;
-#pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                      if (QS == 1 || (w >> 1) == q) kp |= (c->red[s][tb][w][1] != 0.f);
-                    keep[q][1] = kp;
-                  }
+                  const uint4 v2 = *reinterpret_cast<const uint4*>(&c->vote2[s][tb][0]);
+                  uint32_t u0 = v2.x | v2.y, u1 = v2.z | v2.w;
+                  if (QS == 1) u0 = u1 = u0 | u1;
+                  if (cls[0][1] == 1) keep[0][1] = u0 & 1u;
+                  if (cls[1][1] == 1) keep[1][1] = u1 & 1u;
                 }
-                if (keep[myqs][1]) m_true = fmaxf(m_true, rm1);
+                if ((myqs ? keep[1][1] : keep[0][1])) m_true = fmaxf(m_true, rm1);
               }
             }
           }
@@ -599,12 +660,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
           if (leader && my_i * p.Bq < len) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const int cl = cls[myqs][k];
+              const int cl = (myqs ? cls[1][k] : cls[0][k]);
               if (cl == 0) continue;
               const int j = (J * TILE) / p.Bk + k;
               if (cl == 1) {
                 ++cnt_cand;
-                cnt_kept += keep[myqs][k] ? 1 : 0;
+                cnt_kept += (myqs ? keep[1][k] : keep[0][k]) ? 1 : 0;
               } else {
                 ++cnt_diag;
               }
@@ -614,15 +675,15 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                   bm_idx = j >> 5;
                   bm_word = 0;
                 }
-                if (keep[myqs][k]) bm_word |= 1u << (j & 31);
+                if ((myqs ? keep[1][k] : keep[0][k])) bm_word |= 1u << (j & 31);
               }
             }
           }
 
           // ---- online softmax over the kept sub-blocks of this slot
           if (decbits != 0u) {
-            const bool k0 = keep[myqs][0];
-            const bool k1 = (KS == 1) ? k0 : keep[myqs][1];
+            const bool k0 = (myqs ? keep[1][0] : keep[0][0]);
+            const bool k1 = (KS == 1) ? k0 : (myqs ? keep[1][1] : keep[0][1]);
             float rmk = -CUDART_INF_F;
             if (k0) rmk = fmaxf(rmk, rm0);
             if (k1) rmk = fmaxf(rmk, rm1);
@@ -648,8 +709,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             }
             // Pass 2: P = exp2(sigma*log2e*(S - m)) for the kept, visible
             // entries, packed as bf16 pairs into the first 64 columns of the
-            // S region (half hf of S -> P columns [32 hf, 32 hf + 32); those
-            // S columns have already been read).
+            // S region (half hf -> P columns [32 hf, 32 hf + 32); those S
+            // columns have been read by then).
             const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * sc;
             const uint64_t sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
             uint64_t lsum2 = f2_pack(0.f, 0.f);
@@ -657,22 +718,23 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               const bool kk = (hf == 0) ? k0 : k1;
-              uint32_t sr[2][32];
-              tmem_ld32(tS + hf * 64, sr[0]);
-              tmem_ld32(tS + hf * 64 + 32, sr[1]);
+              // Re-read this half of S from TMEM (cheaper than holding the
+              // whole row in registers across the gate).
+              tmem_ld32(tS + hf * 64, sr[2 * hf]);
+              tmem_ld32(tS + hf * 64 + 32, sr[2 * hf + 1]);
               tmem_wait_ld();
               uint32_t pk[32];
               if (fast) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                  const uint64_t x2 = f2_pack(__uint_as_float(sr[e >> 4][(2 * e) & 31]),
-                                              __uint_as_float(sr[e >> 4][(2 * e + 1) & 31]));
+                  const uint64_t x2 = f2_pack(__uint_as_float(sr[2 * hf + (e >> 4)][(2 * e) & 31]),
+                                              __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e + 1) & 31]));
                   float y0, y1;
                   f2_unpack(f2_fma(x2, sc2, nmb2), y0, y1);
                   const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
                   const uint64_t pp = f2_pack(p0, p1);
                   lsum2 = f2_add(lsum2, pp);
-                  pk[e] = pack_bf16x2(p0, p1);
+                  pk[e] = pack_bf16x2_fast(p0, p1);
                 }
               } else {
 #pragma unroll
@@ -680,12 +742,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                   const int cc = hf * 64 + 2 * e;
                   const bool vis0 = kk && !(diag_tile && cc > row);
                   const bool vis1 = kk && !(diag_tile && cc + 1 > row);
-                  const float x0 = __uint_as_float(sr[e >> 4][(2 * e) & 31]);
-                  const float x1 = __uint_as_float(sr[e >> 4][(2 * e + 1) & 31]);
+                  const float x0 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e) & 31]);
+                  const float x1 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e + 1) & 31]);
                   const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
                   const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
                   lsum2 = f2_add(lsum2, f2_pack(p0, p1));
-                  pk[e] = pack_bf16x2(p0, p1);
+                  pk[e] = pack_bf16x2_fast(p0, p1);
                 }
               }
               tmem_st32(tS + hf * 32, pk);

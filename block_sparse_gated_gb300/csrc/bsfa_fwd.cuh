@@ -256,8 +256,14 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
 
-  const int HP = p.Hkv * p.pairs;
-  const int total_units = (*p.ntiles_total) * HP;
+  // Unit order: KV head slowest, then query tiles heaviest first, then the
+  // q-head pairs of the group.  Each wave of resident CTAs then streams one
+  // KV head's K/V prefix, which stays resident in L2 while every CTA of the
+  // wave walks it (with the KV head fastest the wave streamed all heads and
+  // re-read K/V from DRAM many times over).
+  const int ntot = *p.ntiles_total;
+  const int per_kv = ntot * p.pairs;
+  const int total_units = per_kv * p.Hkv;
 
   // Register split for two slots (launched at 168 per thread, 384 threads):
   // warpgroup 0 (copies, MMA issue) gives up to 56, the two softmax
@@ -273,8 +279,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     int last_q = -1;  // index of the last unit whose Q load was issued
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
-      const int2 t = p.tiles[u / HP];
-      const int hp = u % HP, kvh = hp / p.pairs, pr = hp % p.pairs;
+      const int kvh = u / per_kv, rem = u - kvh * per_kv;
+      const int2 t = p.tiles[rem / p.pairs];
+      const int pr = rem % p.pairs;
       const int4 si = p.seqinfo[t.x];
       const int I = t.y, nkt = I + 1;
       const int row0 = si.x + I * TILE;
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
     const uint64_t dV = smem_desc_sw128(smem_u32(sV), HALF, 1024);
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
-      const int2 t = p.tiles[u / HP];
+      const int2 t = p.tiles[(u % per_kv) / p.pairs];
       const int nkt = t.y + 1;
       for (int s = 0; s < NQ && ok; ++s)
         ok = wait_all(&c->q_full[s], uc & 1, abort, p.err, ERR_WAIT_Q_FULL);
@@ -485,8 +492,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     unsigned long long cnt_kept = 0, cnt_cand = 0, cnt_diag = 0;
 
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
-      const int2 t = p.tiles[u / HP];
-      const int hp = u % HP, kvh = hp / p.pairs, pr = hp % p.pairs;
+      const int kvh = u / per_kv, rem = u - kvh * per_kv;
+      const int2 t = p.tiles[rem / p.pairs];
+      const int pr = rem % p.pairs;
       const int4 si = p.seqinfo[t.x];
       const int I = t.y, nkt = I + 1, len = si.y;
       const int h = kvh * p.group + pr * NQ + s;

@@ -34,6 +34,23 @@ METRIC = ("prefill attention ms/layer & effective TFLOPS (frac of bf16 peak) at 
 UNIT = "TFLOP/s (effective)"
 
 
+def _recorded_traffic(workload):
+    """Mean DRAM bytes per launch of the prefill kernel from the committed ncu
+    record, or None when the kernel sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"bsfa_fwd_kernel_dram_{workload}.json")
+    try:
+        rec = json.load(open(path))
+        h = hashlib.sha256()
+        for f in rec["sources"]:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return float(rec["mean_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -244,7 +261,8 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(launch_achieved / peak_sust, 4),
                      "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
                      "frac_of_burst": round(launch_achieved / peak_burst, 4),
-                     "traffic": None},
+                     "traffic": _recorded_traffic(args.workload),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "clocks": clocks,
         "gpu_launches": 2 * len(ks) * args.steps,
         "calibrate": {"ms": round(W["cal_ms"], 3), "samples": cfg["n_cal"],

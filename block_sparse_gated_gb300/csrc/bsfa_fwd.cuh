@@ -33,6 +33,12 @@ constexpr int KST = 2;  // K ring stages
 constexpr int VST = 2;  // V ring stages
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
 constexpr float RESCALE_LOG2 = 8.0f;  // lazy rescale: P may grow to 2^8 before O is rescaled
+// Register split for two slots (384 threads): warpgroup 0 (copies, MMA issue)
+// drops to COPY_REGS, the two softmax warpgroups rise to SOFTMAX_REGS.  The
+// host checks 128*COPY_REGS + 256*SOFTMAX_REGS against the registers the
+// kernel is launched with before the first launch.
+constexpr int COPY_REGS = 56;
+constexpr int SOFTMAX_REGS = 224;
 
 // Device error word codes (site of the wait that ran out).
 enum : unsigned {
@@ -265,14 +271,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
   const int per_kv = ntot * p.pairs;
   const int total_units = per_kv * p.Hkv;
 
-  // Register split for two slots (launched at 168 per thread, 384 threads):
-  // warpgroup 0 (copies, MMA issue) gives up to 56, the two softmax
-  // warpgroups rise to 224: 128*56 + 256*224 = 384*168.  Each role sets its
-  // own limit at the top of its branch.
+  // Register split (two slots): each role sets its own limit at the top of
+  // its branch, so the compiler allocates each branch against its limit.
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if constexpr (NQ == 2) setmaxnreg_dec<56>();
+    if constexpr (NQ == 2) setmaxnreg_dec<COPY_REGS>();
     // The whole warp runs the loop and the waits (so every value it uses is
     // warp-uniform); one elected lane issues each copy.
     uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
-    if constexpr (NQ == 2) setmaxnreg_dec<56>();
+    if constexpr (NQ == 2) setmaxnreg_dec<COPY_REGS>();
     // The whole warp runs the loop and the waits; one elected lane (always
     // the same lane: all 32 are active) issues every MMA and commit, so each
     // commit tracks that lane's earlier MMAs.
@@ -471,10 +475,10 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     __syncwarp();
     drain_wait(&c->drain, 0);
   } else if (warp < 4) {
-    if constexpr (NQ == 2) setmaxnreg_dec<56>();
+    if constexpr (NQ == 2) setmaxnreg_dec<COPY_REGS>();
   } else {
     // -------------------------------------------------------------- softmax
-    if constexpr (NQ == 2) setmaxnreg_inc<224>();
+    if constexpr (NQ == 2) setmaxnreg_inc<SOFTMAX_REGS>();
     const int s = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;

@@ -15,6 +15,16 @@ cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t
   if (dev >= 64 || !configured[dev]) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::BYTES);
     if (e != cudaSuccess) return e;
+    if constexpr (NQ == 2) {
+      // setmaxnreg moves registers between warpgroups inside the block's own
+      // allocation; an increase the allocation cannot cover would never
+      // complete, so refuse to launch rather than risk it.
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return e;
+      if (128 * COPY_REGS + 256 * SOFTMAX_REGS > LY::NTHREADS * fa.numRegs)
+        return cudaErrorInvalidConfiguration;
+    }
     if (dev < 64) configured[dev] = true;
   }
   fn<<<grid, LY::NTHREADS, LY::BYTES, stream>>>(m.q, m.k, m.v, p);

@@ -47,6 +47,7 @@ SIGNATURES = [
         ctypes.POINTER(c_int), c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     ("bsfa_device_error", c_int, [c_void_p, ctypes.POINTER(ctypes.c_uint)]),
     ("bsfa_prefill_fwd_noalloc", c_int, [ctypes.POINTER(FwdParams), c_void_p]),
+    ("bsfa_selftest_wait_guard", c_int, [ctypes.c_uint, c_void_p]),
 ]
 
 _lib = None

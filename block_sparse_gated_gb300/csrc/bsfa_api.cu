@@ -132,6 +132,25 @@ __global__ void __launch_bounds__(1024) select_kernel(const SelectArgs a) {
   }
 }
 
+// ------------------------------------------------------------ hang-guard self test
+// One warp waits, through the attention kernel's own bounded-wait helper, on
+// an mbarrier that nothing ever arrives on.  The wait gives up after
+// timeout_ns, records ERR_WAIT_SELFTEST in the device error word and the
+// kernel returns normally, leaving the context usable.
+__global__ void __launch_bounds__(32) wait_guard_selftest_kernel(unsigned long long timeout_ns,
+                                                                 unsigned* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0)
+    wait_bar(&bar, 0, &abort_flag, err, ERR_WAIT_SELFTEST, timeout_ns);
+}
+
 // ------------------------------------------------------------ TMA descriptors
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -479,6 +498,15 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
     if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;
   }
   return BSFA_OK;
+}
+
+bsfa_status bsfa_selftest_wait_guard(unsigned int timeout_us, bsfa_stream_t stream_) {
+  if (timeout_us == 0 || timeout_us > 10000000u) return BSFA_ERR_INVALID_ARG;
+  unsigned* err = error_word();
+  if (err == nullptr) return BSFA_ERR_CUDA;
+  wait_guard_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(
+      1000ull * timeout_us, err);
+  return cudaGetLastError() == cudaSuccess ? BSFA_OK : BSFA_ERR_CUDA;
 }
 
 bsfa_status bsfa_device_error(bsfa_stream_t stream_, unsigned int* code) {

@@ -44,7 +44,8 @@ constexpr int SOFTMAX_REGS = 224;
 enum : unsigned {
   ERR_WAIT_Q_EMPTY = 0x101, ERR_WAIT_K_EMPTY, ERR_WAIT_V_EMPTY, ERR_WAIT_DEC,
   ERR_WAIT_Q_FULL, ERR_WAIT_K_FULL, ERR_WAIT_V_FULL, ERR_WAIT_P_FULL, ERR_WAIT_O_EMPTY,
-  ERR_WAIT_S_FULL, ERR_WAIT_WG, ERR_WAIT_O_FULL, ERR_WAIT_DRAIN
+  ERR_WAIT_S_FULL, ERR_WAIT_WG, ERR_WAIT_O_FULL, ERR_WAIT_DRAIN,
+  ERR_WAIT_SELFTEST = 0x1FF
 };
 
 struct DevParams {
@@ -108,14 +109,15 @@ struct Layout {
 // Bounded wait: true when the phase of `parity` completed; false after the
 // time bound (error word set, abort raised) or when another role aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                         unsigned* err, unsigned site) {
+                                         unsigned* err, unsigned site,
+                                         uint64_t timeout_ns = WAIT_TIMEOUT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 31u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > WAIT_TIMEOUT_NS) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
         *abort = 1;
         atomicCAS(err, 0u, site);
         return false;

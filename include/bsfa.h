@@ -104,7 +104,8 @@ typedef struct {
                                  scaled scores; -inf keeps everything */
   int thresholds_nq;          /* nT >= 1; query blocks i >= nT use T[h][nT-1] */
   float log_lambda;           /* natural log of lambda (LAMBDA mode) */
-  uint32_t* kept_bitmap;      /* nullable device output, see bsfa_bitmap_shape: bit j of
+  uint32_t* kept_bitmap;      /* nullable device output [rows][Hq][words_per_row] (see
+                                 bsfa_bitmap_words_per_row): bit j of
                                  row (h, row_base(b) + i) = keep(i,j); diagonal-region bits
                                  are 1; invisible blocks 0; every word of every row written */
   float* lse;                 /* nullable device fp32 output [Hq][rows]: natural-log
@@ -197,6 +198,14 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
  * none).  Returns BSFA_ERR_DEVICE_TIMEOUT if it was set, BSFA_ERR_CUDA if the
  * synchronisation failed, else BSFA_OK. */
 bsfa_status bsfa_device_error(bsfa_stream_t stream, unsigned int* code);
+
+/* Hang-guard self test.  Launches one warp on `stream` that waits, through
+ * the same bounded-wait routine the attention kernels use, on a barrier that
+ * nothing ever completes.  After timeout_us microseconds (1 .. 10^7) the wait
+ * gives up, records code 0x1FF in the device error word and the kernel exits
+ * normally.  bsfa_device_error then returns BSFA_ERR_DEVICE_TIMEOUT with that
+ * code, and the context stays usable.  No fault, trap or hang is involved. */
+bsfa_status bsfa_selftest_wait_guard(unsigned int timeout_us, bsfa_stream_t stream);
 
 /* Static description of a status code. */
 const char* bsfa_status_string(bsfa_status s);

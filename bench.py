@@ -271,6 +271,8 @@ def run_ours(args, rank, world, local_rank):
 
     if not args.no_sweep and rank == 0:
         result["lambda_sweep"] = lambda_sweep(dev, args)
+        result["llama8b_L32768"] = llama_32k_leg(dev)
+        result["varlen_8seq_32layer"] = varlen_32layer_leg(dev)
     if not args.no_e2e:
         result["e2e"] = e2e(q, k, v, slices, flops, Bq, Bk, args, dev)
     if not args.no_cpu and rank == 0 and world == 1:
@@ -399,6 +401,99 @@ def lambda_sweep(dev, args):
             "zero_skip_overhead_lambda": round(rows[0]["ms"] / base - 1, 4),
             "zero_skip_overhead_threshold": round(rows[0]["ms_threshold_minus_inf"] / base - 1, 4),
             "monotonic": all(a > b for a, b in zip(times, times[1:]))}
+
+
+def _timed(fn, reps):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def llama_32k_leg(dev, reps=5):
+    """The 32K layer: thresholds calibrated on 4 x 32K samples, k = 64."""
+    import torch
+
+    import block_sparse_gated_gb300 as bsfa
+    W = build_workload("llama8b-L32768", dev)
+    cfg = W["cfg"]
+    q, k, v, T = W["q"][None], W["k"][None], W["v"][None], W["T"][0].contiguous()
+    out = torch.empty_like(q)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    r = bsfa.prefill(q, k, v, mode="threshold", thresholds=T, out=out, workspace=ws,
+                     return_counts=True)
+    torch.cuda.synchronize()
+    kc, cand, diag = r["counts"].cpu().tolist()
+    ms = _timed(lambda: bsfa.prefill(q, k, v, mode="threshold", thresholds=T, out=out,
+                                     workspace=ws), reps)
+    fl = effective_flops((kc, cand, diag), cfg["Bq"], cfg["Bk"], cfg["d"])
+    return {"workload": "llama8b-L32768", "k": cfg["ks"][0], "ms_per_layer": round(ms, 3),
+            "skip_rate": round(1 - kc / cand, 4),
+            "effective_tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+            "calibrate_ms": round(W["cal_ms"], 3)}
+
+
+def varlen_32layer_leg(dev):
+    """8 sequences (4K..64K) packed with cu_seqlens; one threshold table per
+    layer (k = 128, 4 x 64K calibration samples per layer); the 32 layers'
+    slices run back to back over the packed batch (per-layer time = total / 32)."""
+    import torch
+
+    import block_sparse_gated_gb300 as bsfa
+    from block_sparse_gated_gb300 import workloads as wl
+    cfg = wl.WORKLOADS["varlen-8seq-32layer"]
+    Hq, Hkv, d, B = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["Bk"]
+    tables = []
+    t_cal = 0.0
+    for layer in range(cfg["layers"]):
+        cal = [wl.layer_inputs(Hq, Hkv, cfg["cal_L"], d, wl.cal_seed(cfg["index"], n, layer), dev,
+                               with_v=False, sink_tokens=cfg["sink_tokens"],
+                               needles=cfg["cal_needles"], block=B) for n in range(cfg["n_cal"])]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        T = bsfa.calibrate([c.q for c in cal], [c.k for c in cal], cfg["ks"], block_q=B,
+                           block_k=B)
+        e1.record()
+        torch.cuda.synchronize()
+        t_cal += e0.elapsed_time(e1)
+        tables.append(T[0].contiguous())
+        del cal
+    lens = cfg["lens"]
+    parts = [wl.layer_inputs(Hq, Hkv, Ln, d, wl.eval_seed(cfg["index"], n), dev,
+                             sink_tokens=cfg["sink_tokens"],
+                             needles=max(1, round(cfg["needles_per_64k"] * Ln / 65536)), block=B)
+             for n, Ln in enumerate(lens)]
+    q, cu = wl.pack_varlen([p_.q for p_ in parts])
+    k, _ = wl.pack_varlen([p_.k for p_ in parts])
+    v, _ = wl.pack_varlen([p_.v for p_ in parts])
+    del parts
+    cu = cu.to(dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    tot = [0, 0, 0]
+    for T in tables:
+        r = bsfa.prefill(q, k, v, cu_seqlens=cu, max_seqlen=max(lens), mode="threshold",
+                         thresholds=T, out=out, workspace=ws, return_counts=True)
+        torch.cuda.synchronize()
+        tot = [a + b for a, b in zip(tot, r["counts"].cpu().tolist())]
+
+    def all_layers():
+        for T in tables:
+            bsfa.prefill(q, k, v, cu_seqlens=cu, max_seqlen=max(lens), mode="threshold",
+                         thresholds=T, out=out, workspace=ws)
+
+    ms = _timed(all_layers, 2)
+    fl = effective_flops(tot, B, B, d)
+    return {"workload": "varlen-8seq-32layer", "tokens": int(sum(lens)), "layers": len(tables),
+            "ms_per_layer": round(ms / len(tables), 3), "skip_rate": round(1 - tot[0] / tot[1], 4),
+            "effective_tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+            "calibrate_ms_per_layer": round(t_cal / len(tables), 3)}
 
 
 # --------------------------------------------------------------- CPU oracle

@@ -37,8 +37,8 @@ constexpr float RESCALE_LOG2 = 8.0f;  // lazy rescale: P may grow to 2^8 before 
 // drops to COPY_REGS, the two softmax warpgroups rise to SOFTMAX_REGS.  The
 // host checks 128*COPY_REGS + 256*SOFTMAX_REGS against the registers the
 // kernel is launched with before the first launch.
-constexpr int COPY_REGS = 56;
-constexpr int SOFTMAX_REGS = 224;
+constexpr int COPY_REGS = 104;
+constexpr int SOFTMAX_REGS = 200;
 
 // Device error word codes (site of the wait that ran out).
 enum : unsigned {
@@ -173,6 +173,20 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t n, bool pred) 
   return r != 0;
 }
 
+// Barrier over the `n` threads of a warpgroup that counts the threads whose
+// predicate is true.
+__device__ __forceinline__ uint32_t bar_red_popc(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.popc.u32 %0, %2, %3, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r;
+}
+
 // Semantic block class of key block j for query block i (length-L sequence):
 // 1 = candidate (every key precedes every row), 2 = diagonal region, 0 = none.
 __device__ __forceinline__ int block_class(int i, int j, int Bq, int Bk, int L) {
@@ -234,8 +248,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       mbar_init(&c->p_full[s], 128);
       mbar_init(&c->o_full[s], 1);
       mbar_init(&c->o_empty[s], 128);
-      mbar_init(&c->dec_full[s][0], 1);
-      mbar_init(&c->dec_full[s][1], 1);
+      mbar_init(&c->dec_full[s][0], 32);
+      mbar_init(&c->dec_full[s][1], 32);
     }
     mbar_init(&c->q_empty, 1);
     for (int i = 0; i < KST; ++i) {
@@ -407,12 +421,17 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         const uint32_t kst = kc % KST;
         bool vready = false, any = false;
         for (int s = 0; s < NQ; ++s) {
-          if (!(ok = wait_all(&c->p_full[s], tc & 1, abort, p.err, ERR_WAIT_P_FULL))) break;
-          tc_fence_after();
           bool do_pv = false;
           uint32_t acc = 1u;
           if constexpr (!CALIB) {
-            const uint32_t dec = GATING ? c->dec[s][tb] : 1u;
+            // The decision is published after pass 1, well before P: read it
+            // (and wait for V and O) while the softmax is still writing P.
+            uint32_t dec = 1u;
+            if constexpr (GATING) {
+              if (!(ok = wait_all(&c->dec_full[s][tb], (tc >> 1) & 1, abort, p.err, ERR_WAIT_DEC)))
+                break;
+              dec = c->dec[s][tb];
+            }
             if (dec != 0u) {
               any = true;
               do_pv = true;
@@ -434,6 +453,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
               }
             }
           }
+          if (!(ok = wait_all(&c->p_full[s], tc & 1, abort, p.err, ERR_WAIT_P_FULL))) break;
+          tc_fence_after();
           const bool do_qk = J + 1 < nkt;
           // P.V for this tile first: it does not need the next K tile.
           if (do_pv && elect_one())
@@ -491,7 +512,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     const int QS = TILE / p.Bq, KS = TILE / p.Bk;
     const bool simple = (QS == 1 && KS == 1);  // one semantic block per 128x128 tile
     const int myqs = (p.Bq == 64) ? (row >> 6) : 0;
-    const bool leader = (row % p.Bq) == 0;  // first row of its semantic query block
+    // The warp holding the first row of a semantic query block keeps that
+    // block's counts and bitmap words.  Every lane of it keeps the same
+    // values (gate decisions are warp-uniform), so the bookkeeping never
+    // splits the warp (a one-lane branch here slowed the whole warp's
+    // exp pass); lane 0 alone stores.
+    const bool lead_warp = ((wq * 32) % p.Bq) == 0;
     const float sc = p.sigma_log2;
     uint32_t tc = 0, uc = 0;
     bool ok = true;
@@ -517,7 +543,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       bool o_init = false;
       uint32_t bm_word = 0;
       int bm_idx = 0;
-      const bool bm_on = (p.bitmap != nullptr) && leader && (my_i * p.Bq < len);
+      const bool bm_on = (p.bitmap != nullptr) && lead_warp && (my_i * p.Bq < len);
       const long long bm_row = ((long long)(si.z + my_i) * p.Hq + h) * (long long)p.words;
 
       for (int J = 0; J < nkt; ++J, ++tc) {
@@ -581,13 +607,16 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         // sigma * (rowmax_r - m_r) >= ln(lambda).  One barrier per tile also
         // settles whether every thread of the warpgroup is still running.
         const bool lambda_mode = GATING && !CALIB && p.mode == 1;
+        // One 128x128 semantic block per tile: the barrier itself carries the
+        // vote.  Lane 0 of each warp counts 1 when some lane of the warp has
+        // stopped, lanes 1..8 count 1 each when some row of the warp wants the
+        // block, so the count is F + 8 V with F, V <= 4.
+        bool tile_vote = false;
         if constexpr (CALIB) {
           const float w0 = warp_max_f32(rvalid ? rm0 : -CUDART_INF_F);
           const float w1 = (KS == 1) ? w0 : warp_max_f32(rvalid ? rm1 : -CUDART_INF_F);
-          if (lane == 0) {
-            c->red[s][tb][wq][0] = w0;
-            c->red[s][tb][wq][1] = w1;
-          }
+          c->red[s][tb][wq][0] = w0;  // every lane: same value
+          c->red[s][tb][wq][1] = w1;
         } else if constexpr (GATING) {
           bool w0, w1 = false;
           if (!lambda_mode) {
@@ -597,11 +626,23 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
           } else {
             w0 = rvalid && (myqs ? cls[1][0] : cls[0][0]) == 1 && ((rm0 - m_true) * p.sigma >= p.log_lambda);
           }
-          const uint32_t bits = (__any_sync(0xffffffffu, w0) ? 1u : 0u) |
-                                ((KS == 2 && __any_sync(0xffffffffu, w1)) ? 2u : 0u);
-          if (lane == 0) c->vote[s][tb][wq] = bits;
+          if (simple) {
+            const bool wf = __any_sync(0xffffffffu, !okl);
+            const bool wv = __any_sync(0xffffffffu, w0);
+            const uint32_t n = bar_red_popc(bar_id, 128, lane == 0 ? wf : (lane <= 8 && wv));
+            ok = (n & 7u) == 0u;
+            if (!ok) break;
+            tile_vote = n >= 8u;
+          } else {
+            const uint32_t bits = (__any_sync(0xffffffffu, w0) ? 1u : 0u) |
+                                  ((KS == 2 && __any_sync(0xffffffffu, w1)) ? 2u : 0u);
+            c->vote[s][tb][wq] = bits;  // every lane: same value
+          }
         }
-        if (!(ok = bar_red_and(bar_id, 128, okl))) break;
+        if (!(GATING && !CALIB && simple)) {
+          ok = bar_red_and(bar_id, 128, okl);
+          if (!ok) break;
+        }
 
         if constexpr (CALIB) {
           // Calibration: record sigma * s_max for candidate blocks.
@@ -629,9 +670,15 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             for (int k = 0; k < 2; ++k) keep[q][k] = cls[q][k] != 0;
           if constexpr (GATING) {
             // OR the warp votes of each query half (warps 0-1 hold rows 0-63).
-            const uint4 vv = *reinterpret_cast<const uint4*>(&c->vote[s][tb][0]);
-            uint32_t vq0 = vv.x | vv.y, vq1 = vv.z | vv.w;
-            if (QS == 1) vq0 = vq1 = vq0 | vq1;
+            uint32_t vq0, vq1;
+            if (simple) {
+              vq0 = vq1 = tile_vote ? 1u : 0u;
+            } else {
+              const uint4 vv = *reinterpret_cast<const uint4*>(&c->vote[s][tb][0]);
+              vq0 = vv.x | vv.y;
+              vq1 = vv.z | vv.w;
+              if (QS == 1) vq0 = vq1 = vq0 | vq1;
+            }
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               if (cls[0][k] == 1) keep[0][k] = (vq0 >> k) & 1u;
@@ -647,7 +694,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                   const bool w1 =
                       rvalid && (myqs ? cls[1][1] : cls[0][1]) == 1 && ((rm1 - m_true) * p.sigma >= p.log_lambda);
                   const uint32_t b1 = __any_sync(0xffffffffu, w1) ? 1u : 0u;
-                  if (lane == 0) c->vote2[s][tb][wq] = b1;
+                  c->vote2[s][tb][wq] = b1;
                   named_bar_sync(bar_id, 128);
                   const uint4 v2 = *reinterpret_cast<const uint4*>(&c->vote2[s][tb][0]);
                   uint32_t u0 = v2.x | v2.y, u1 = v2.z | v2.w;
@@ -665,33 +712,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 #pragma unroll
             for (int k = 0; k < 2; ++k)
               if (keep[q][k]) decbits |= 1u << (q * 2 + k);
-          if (GATING && row == 0) {
+          if (GATING && wq == 0) {  // all 32 lanes: same value, 32 arrivals
             c->dec[s][tb] = decbits;
             mbar_arrive(&c->dec_full[s][tb]);
-          }
-
-          // ---- bookkeeping: bitmap words and block counts
-          if (leader && my_i * p.Bq < len) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int cl = (myqs ? cls[1][k] : cls[0][k]);
-              if (cl == 0) continue;
-              const int j = (J * TILE) / p.Bk + k;
-              if (cl == 1) {
-                ++cnt_cand;
-                cnt_kept += (myqs ? keep[1][k] : keep[0][k]) ? 1 : 0;
-              } else {
-                ++cnt_diag;
-              }
-              if (bm_on) {
-                if ((j >> 5) != bm_idx) {
-                  p.bitmap[bm_row + bm_idx] = bm_word;
-                  bm_idx = j >> 5;
-                  bm_word = 0;
-                }
-                if ((myqs ? keep[1][k] : keep[0][k])) bm_word |= 1u << (j & 31);
-              }
-            }
           }
 
           // ---- online softmax over the kept sub-blocks of this slot
@@ -774,16 +797,40 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
           }
           tc_fence_before();
           mbar_arrive(&c->p_full[s]);
+
+          // ---- bookkeeping: bitmap words and block counts (after the
+          // hand-off of P, off the path to the next MMA)
+          if (lead_warp && my_i * p.Bq < len) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int cl = (myqs ? cls[1][k] : cls[0][k]);
+              if (cl == 0) continue;
+              const int j = (J * TILE) / p.Bk + k;
+              if (cl == 1) {
+                ++cnt_cand;
+                cnt_kept += (myqs ? keep[1][k] : keep[0][k]) ? 1 : 0;
+              } else {
+                ++cnt_diag;
+              }
+              if (bm_on) {
+                if ((j >> 5) != bm_idx) {
+                  if (lane == 0) p.bitmap[bm_row + bm_idx] = bm_word;
+                  bm_idx = j >> 5;
+                  bm_word = 0;
+                }
+                if ((myqs ? keep[1][k] : keep[0][k])) bm_word |= 1u << (j & 31);
+              }
+            }
+          }
         }
       }
       if (!ok) break;
 
       if constexpr (!CALIB) {
         // ---- epilogue: O / l -> bf16, log-sum-exp, bitmap tail
-        if (bm_on) {
-          p.bitmap[bm_row + bm_idx] = bm_word;
-          for (int w = bm_idx + 1; w < p.words; ++w) p.bitmap[bm_row + w] = 0u;
-        }
+        if (bm_on)
+          for (int w = bm_idx + lane; w < p.words; w += 32)
+            p.bitmap[bm_row + w] = (w == bm_idx) ? bm_word : 0u;
         const bool okl = wait_bar(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL);
         if (!(ok = bar_red_and(bar_id, 128, okl))) break;
         tc_fence_after();
@@ -815,7 +862,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         mbar_arrive(&c->o_empty[s]);
       }
     }
-    if (p.counts != nullptr && (cnt_cand | cnt_diag) != 0ull) {
+    if (p.counts != nullptr && lane == 0 && (cnt_cand | cnt_diag) != 0ull) {
       atomicAdd(&p.counts[0], cnt_kept);
       atomicAdd(&p.counts[1], cnt_cand);
       atomicAdd(&p.counts[2], cnt_diag);

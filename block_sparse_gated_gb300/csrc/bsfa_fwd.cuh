@@ -453,7 +453,13 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
               }
             }
           }
-          if (!(ok = wait_all(&c->p_full[s], tc & 1, abort, p.err, ERR_WAIT_P_FULL))) break;
+          // A skipped tile has no P: its S was read before the decision was
+          // published, so the next S may be issued now.  (The next decision
+          // is published only after every thread has arrived on p_full for
+          // this tile, so this phase completes before the next wait on it.)
+          if (CALIB || !GATING || do_pv) {
+            if (!(ok = wait_all(&c->p_full[s], tc & 1, abort, p.err, ERR_WAIT_P_FULL))) break;
+          }
           tc_fence_after();
           const bool do_qk = J + 1 < nkt;
           // P.V for this tile first: it does not need the next K tile.
@@ -626,6 +632,10 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
           } else {
             w0 = rvalid && (myqs ? cls[1][0] : cls[0][0]) == 1 && ((rm0 - m_true) * p.sigma >= p.log_lambda);
           }
+          // Every read of S is complete here (tcgen05.wait::ld above); the
+          // fence orders it before the barrier, so that the MMA warp may
+          // overwrite S as soon as it reads a skip decision.
+          tc_fence_before();
           if (simple) {
             const bool wf = __any_sync(0xffffffffu, !okl);
             const bool wv = __any_sync(0xffffffffu, w0);

@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                   const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
                   const uint64_t pp = f2_pack(p0, p1);
                   lsum2 = f2_add(lsum2, pp);
-                  pk[e] = pack_bf16x2_fast(p0, p1);
+                  pk[e] = pack_bf16x2(p0, p1);
                 }
               } else {
 #pragma unroll
@@ -794,7 +794,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                   const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
                   const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
                   lsum2 = f2_add(lsum2, f2_pack(p0, p1));
-                  pk[e] = pack_bf16x2_fast(p0, p1);
+                  pk[e] = pack_bf16x2(p0, p1);
                 }
               }
               tmem_st32(tS + hf * 32, pk);

@@ -224,17 +224,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
-// bf16 pair from two finite, non-negative fp32 values using integer ops only
-// (keeps the packing off the quarter-rate conversion pipe): add half an ulp
-// of bf16 to the fp32 bit pattern and keep the upper 16 bits of each
-// (round half up; it differs from round-to-nearest-even only on exact ties).
-__device__ __forceinline__ uint32_t pack_bf16x2_fast(float lo, float hi) {
-  const uint32_t a = __float_as_uint(lo) + 0x8000u, b = __float_as_uint(hi) + 0x8000u;
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -10,8 +10,10 @@
 // running max, the normaliser and O untouched and its V is never fetched.
 //
 // Roles (one CTA per SM, persistent over a heaviest-first unit list):
-//   warp 0          TMA producer: Q per unit, K for every visible tile, V for
-//                   tiles that some slot keeps (issued after the decision).
+//   warp 0          TMA producer: Q per unit, K for every visible tile (and V
+//                   for every tile when the gate is compiled out).
+//   warp 3          (gate on) V loader: V for the tiles that some slot keeps,
+//                   issued as soon as the decision is published.
 //   warp 1          MMA issuer (one thread): S_s = Q_s K^T, O_s += P_s V.
 //                   Also owns the TMEM allocation.
 //   warps 4..       one softmax warpgroup per query slot s (NQ slots = NQ
@@ -333,22 +335,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
           ++kc;
         }
         if (J < 0) continue;
-        if constexpr (!CALIB) {
-          bool need = true;
-          if constexpr (GATING) {
-            need = false;
-            for (int s = 0; s < NQ; ++s) {
-              if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
-                                  ERR_WAIT_DEC)))
-                break;
-              if (c->dec[s][tc & 1] != 0u) {
-                need = true;
-                break;
-              }
-            }
-            if (!ok) break;
-          }
-          if (need) {
+        if constexpr (!CALIB && !GATING) {
+          {
             const uint32_t st = vc % VST;
             if (!(ok = wait_all(&c->v_empty[st], ((vc / VST) & 1) ^ 1, abort, p.err,
                                 ERR_WAIT_V_EMPTY)))
@@ -373,6 +361,52 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         const uint32_t f = kc - 1 - i;
         drain_wait(&c->k_full[f % KST], (f / KST) & 1);
       }
+      for (uint32_t i = 0; i < VST && i < vc; ++i) {
+        const uint32_t f = vc - 1 - i;
+        drain_wait(&c->v_full[f % VST], (f / VST) & 1);
+      }
+    }
+  } else if (GATING && !CALIB && warp == 3) {
+    // ----------------------------------------------------- V loader (gated)
+    // A warp of its own, so that a kept tile's V is requested as soon as a
+    // slot publishes its decision (the producer is busy with K then).
+    if constexpr (NQ == 2) setmaxnreg_dec<COPY_REGS>();
+    uint32_t vc = 0, tc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      const int kvh = u / per_kv, rem = u - kvh * per_kv;
+      const int2 t = p.tiles[rem / p.pairs];
+      const int4 si = p.seqinfo[t.x];
+      const int nkt = t.y + 1;
+      for (int J = 0; J < nkt; ++J, ++tc) {
+        bool need = false;
+        for (int s = 0; s < NQ; ++s) {
+          if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
+                              ERR_WAIT_DEC)))
+            break;
+          if (c->dec[s][tc & 1] != 0u) {
+            need = true;
+            break;
+          }
+        }
+        if (!ok) break;
+        if (need) {
+          const uint32_t st = vc % VST;
+          if (!(ok = wait_all(&c->v_empty[st], ((vc / VST) & 1) ^ 1, abort, p.err,
+                              ERR_WAIT_V_EMPTY)))
+            break;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&c->v_full[st], TB);
+            for (int hf = 0; hf < NHALF; ++hf)
+              tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64,
+                          si.x + J * TILE, kvh, si.w);
+          }
+          __syncwarp();
+          ++vc;
+        }
+      }
+    }
+    if (!ok) {
       for (uint32_t i = 0; i < VST && i < vc; ++i) {
         const uint32_t f = vc - 1 - i;
         drain_wait(&c->v_full[f % VST], (f / VST) & 1);

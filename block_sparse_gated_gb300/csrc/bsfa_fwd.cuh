@@ -379,18 +379,17 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       const int4 si = p.seqinfo[t.x];
       const int nkt = t.y + 1;
       for (int J = 0; J < nkt; ++J, ++tc) {
-        bool need = false;
-        for (int s = 0; s < NQ; ++s) {
+        // Every slot's decision is read on every tile (V is issued on the
+        // first one that keeps the tile), so this warp consumes each
+        // decision phase in order instead of skipping some.
+        bool need = false, issued = false;
+        for (int s = 0; s < NQ && ok; ++s) {
           if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
                               ERR_WAIT_DEC)))
             break;
-          if (c->dec[s][tc & 1] != 0u) {
-            need = true;
-            break;
-          }
-        }
-        if (!ok) break;
-        if (need) {
+          need = need || c->dec[s][tc & 1] != 0u;
+          if (!need || issued) continue;
+          issued = true;
           const uint32_t st = vc % VST;
           if (!(ok = wait_all(&c->v_empty[st], ((vc / VST) & 1) ^ 1, abort, p.err,
                               ERR_WAIT_V_EMPTY)))
@@ -404,6 +403,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
           __syncwarp();
           ++vc;
         }
+        if (!ok) break;
       }
     }
     if (!ok) {

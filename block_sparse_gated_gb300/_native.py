@@ -30,7 +30,12 @@ class FwdParams(ctypes.Structure):
         ("log_lambda", c_float),
         ("kept_bitmap", c_void_p), ("lse", c_void_p), ("block_counts", c_void_p),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+        ("dtype", c_int),
     ]
+
+
+# bsfa_dtype
+DTYPE_BF16, DTYPE_F16 = 0, 1
 
 
 # Every exported symbol and its C signature: (name, restype, argtypes).
@@ -43,7 +48,7 @@ SIGNATURES = [
     ("bsfa_calibrate_workspace_size", c_size_t, [c_int, c_int, c_int, c_int]),
     ("bsfa_calibrate", c_int, [
         ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_int, c_int, c_int, c_int, c_int,
-        ctypes.POINTER(c_int64), ctypes.POINTER(c_int64), c_int, c_int, c_float,
+        c_int, ctypes.POINTER(c_int64), ctypes.POINTER(c_int64), c_int, c_int, c_float,
         ctypes.POINTER(c_int), c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     ("bsfa_device_error", c_int, [c_void_p, ctypes.POINTER(ctypes.c_uint)]),
     ("bsfa_prefill_fwd_noalloc", c_int, [ctypes.POINTER(FwdParams), c_void_p]),

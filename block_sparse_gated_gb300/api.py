@@ -38,10 +38,18 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+_DTYPES = {torch.bfloat16: _native.DTYPE_BF16, torch.float16: _native.DTYPE_F16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError("expected a bfloat16 or float16 tensor")
+    return _DTYPES[t.dtype]
+
+
 def _strides_bhtd(t: torch.Tensor, layout: str, varlen: bool):
-    """Element strides {batch, head, token} of a bf16 tensor with d contiguous."""
-    if t.dtype != torch.bfloat16:
-        raise TypeError("expected a bfloat16 tensor")
+    """Element strides {batch, head, token} of a bf16/fp16 tensor with d contiguous."""
+    _dtype_code(t)
     if t.stride(-1) != 1:
         raise ValueError("the head dimension must be contiguous")
     s = t.stride()
@@ -75,6 +83,8 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
     os_, Ho, Lo = _strides_bhtd(o, layout, varlen)
     if not (Lq == Lk == Lv == Lo) or Hv != Hkv or Ho != Hq:
         raise ValueError("Q/K/V/O shapes disagree")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype):
+        raise TypeError("Q, K, V and O must share one element type")
     d = q.shape[-1]
     p = _native.FwdParams()
     p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
@@ -98,6 +108,7 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
     else:
         p.thresholds, p.thresholds_nq = None, 0
     p.log_lambda = float(log_lambda) if log_lambda is not None else 0.0
+    p.dtype = _dtype_code(q)
     return p
 
 
@@ -172,7 +183,7 @@ def prefill_workspace_bytes(q, k, v, **kw) -> int:
 def calibrate(q_samples, k_samples, ks, *, block_q=128, block_k=128, softmax_scale=None,
               out=None, workspace=None, stream=None):
     """Thresholds [len(ks), Hq, ceil(L/Bq)] (float32, device) from equal-length
-    samples q [Hq, L, d] / k [Hkv, L, d] (bf16, d contiguous)."""
+    samples q [Hq, L, d] / k [Hkv, L, d] (bf16 or fp16, one type for all, d contiguous)."""
     n = len(q_samples)
     if n == 0 or n != len(k_samples):
         raise ValueError("need matching non-empty sample lists")
@@ -180,8 +191,9 @@ def calibrate(q_samples, k_samples, ks, *, block_q=128, block_k=128, softmax_sca
     Hq, Ltok, d = q0.shape
     Hkv = k0.shape[0]
     for t in list(q_samples) + list(k_samples):
-        if t.dtype != torch.bfloat16 or t.stride(-1) != 1 or t.shape[1] != Ltok or t.shape[2] != d:
-            raise ValueError("samples must be bf16 [H, L, d] with d contiguous and equal L")
+        if t.dtype != q0.dtype or t.stride(-1) != 1 or t.shape[1] != Ltok or t.shape[2] != d:
+            raise ValueError("samples must be [H, L, d] of one type with d contiguous and equal L")
+    dcode = _dtype_code(q0)
     nq = (Ltok + block_q - 1) // block_q
     if out is None:
         out = torch.empty((len(ks), Hq, nq), dtype=torch.float32, device=q0.device)
@@ -201,7 +213,7 @@ def calibrate(q_samples, k_samples, ks, *, block_q=128, block_k=128, softmax_sca
             raise ValueError("all k samples must share strides")
     karr = (ctypes.c_int * len(ks))(*[int(x) for x in ks])
     scale = float(softmax_scale) if softmax_scale else 0.0
-    _check(L.bsfa_calibrate(qp, kp, n, Hq, Hkv, Ltok, d, qst, kst, block_q, block_k, scale,
+    _check(L.bsfa_calibrate(qp, kp, n, Hq, Hkv, Ltok, d, dcode, qst, kst, block_q, block_k, scale,
                             karr, len(ks), ctypes.c_void_p(out.data_ptr()),
                             ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                             _stream(stream)), "bsfa_calibrate")

@@ -171,9 +171,10 @@ static EncodeTiled get_encoder() {
   return fn;
 }
 
-// 4-D bf16 map {d, tokens, heads, batch}, box {64, 128, 1, 1}, 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* ptr, int d, long long tokens, int heads, int batch,
-                     long long st_tok, long long st_head, long long st_batch) {
+// 4-D map of 16-bit elements (bf16 or fp16) {d, tokens, heads, batch}, box {64, 128, 1, 1},
+// 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* ptr, bool f16, int d, long long tokens, int heads,
+                     int batch, long long st_tok, long long st_head, long long st_batch) {
   EncodeTiled enc = get_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)tokens, (cuuint64_t)heads, (cuuint64_t)batch};
@@ -181,7 +182,7 @@ static bool make_map(CUtensorMap* m, const void* ptr, int d, long long tokens, i
                            (cuuint64_t)st_batch * 2};
   cuuint32_t box[4] = {64, (cuuint32_t)TILE, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+  return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -199,25 +200,32 @@ static unsigned* error_word() {
   return static_cast<unsigned*>(ptr);
 }
 
-template <bool CALIB>
-static cudaError_t dispatch(int d, int nq, bool gating, const Maps& m, const DevParams& p,
+template <bool CALIB, bool F16>
+static cudaError_t dispatch_t(int d, int nq, bool gating, const Maps& m, const DevParams& p,
                             int grid, cudaStream_t st) {
   if (CALIB) {
-    if (d == 128) return nq == 2 ? launch_fwd<128, 2, true, true>(m, p, grid, st)
-                                 : launch_fwd<128, 1, true, true>(m, p, grid, st);
-    return nq == 2 ? launch_fwd<64, 2, true, true>(m, p, grid, st)
-                   : launch_fwd<64, 1, true, true>(m, p, grid, st);
+    if (d == 128) return nq == 2 ? launch_fwd<128, 2, true, true, F16>(m, p, grid, st)
+                                 : launch_fwd<128, 1, true, true, F16>(m, p, grid, st);
+    return nq == 2 ? launch_fwd<64, 2, true, true, F16>(m, p, grid, st)
+                   : launch_fwd<64, 1, true, true, F16>(m, p, grid, st);
   }
   if (d == 128) {
-    if (gating) return nq == 2 ? launch_fwd<128, 2, true, false>(m, p, grid, st)
-                               : launch_fwd<128, 1, true, false>(m, p, grid, st);
-    return nq == 2 ? launch_fwd<128, 2, false, false>(m, p, grid, st)
-                   : launch_fwd<128, 1, false, false>(m, p, grid, st);
+    if (gating) return nq == 2 ? launch_fwd<128, 2, true, false, F16>(m, p, grid, st)
+                               : launch_fwd<128, 1, true, false, F16>(m, p, grid, st);
+    return nq == 2 ? launch_fwd<128, 2, false, false, F16>(m, p, grid, st)
+                   : launch_fwd<128, 1, false, false, F16>(m, p, grid, st);
   }
-  if (gating) return nq == 2 ? launch_fwd<64, 2, true, false>(m, p, grid, st)
-                             : launch_fwd<64, 1, true, false>(m, p, grid, st);
-  return nq == 2 ? launch_fwd<64, 2, false, false>(m, p, grid, st)
-                 : launch_fwd<64, 1, false, false>(m, p, grid, st);
+  if (gating) return nq == 2 ? launch_fwd<64, 2, true, false, F16>(m, p, grid, st)
+                             : launch_fwd<64, 1, true, false, F16>(m, p, grid, st);
+  return nq == 2 ? launch_fwd<64, 2, false, false, F16>(m, p, grid, st)
+                 : launch_fwd<64, 1, false, false, F16>(m, p, grid, st);
+}
+
+template <bool CALIB>
+static cudaError_t dispatch(bool f16, int d, int nq, bool gating, const Maps& m,
+                            const DevParams& p, int grid, cudaStream_t st) {
+  return f16 ? dispatch_t<CALIB, true>(d, nq, gating, m, p, grid, st)
+             : dispatch_t<CALIB, false>(d, nq, gating, m, p, grid, st);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -263,6 +271,7 @@ static bsfa_status validate(const bsfa_fwd_params* p) {
   if (p->num_heads_q <= 0 || p->num_heads_kv <= 0 || p->num_heads_q % p->num_heads_kv)
     return BSFA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return BSFA_ERR_UNSUPPORTED;
+  if (p->dtype != BSFA_DTYPE_BF16 && p->dtype != BSFA_DTYPE_F16) return BSFA_ERR_UNSUPPORTED;
   if ((p->block_q != 64 && p->block_q != 128) || (p->block_k != 64 && p->block_k != 128))
     return BSFA_ERR_UNSUPPORTED;
   if (p->mode < BSFA_GATE_THRESHOLD || p->mode > BSFA_GATE_NONE) return BSFA_ERR_INVALID_ARG;
@@ -341,16 +350,17 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   auto bstride = [&](const int64_t* st, int heads) {
     return varlen ? (long long)st[1] * heads : (long long)st[0];
   };
-  if (!make_map(&m.q, p->q, d, p->seqlen, p->num_heads_q, bdim, p->q_stride[2], p->q_stride[1],
+  const bool f16 = p->dtype == BSFA_DTYPE_F16;
+  if (!make_map(&m.q, p->q, f16, d, p->seqlen, p->num_heads_q, bdim, p->q_stride[2], p->q_stride[1],
                 bstride(p->q_stride, p->num_heads_q)) ||
-      !make_map(&m.k, p->k, d, p->seqlen, p->num_heads_kv, bdim, p->k_stride[2], p->k_stride[1],
+      !make_map(&m.k, p->k, f16, d, p->seqlen, p->num_heads_kv, bdim, p->k_stride[2], p->k_stride[1],
                 bstride(p->k_stride, p->num_heads_kv)) ||
-      !make_map(&m.v, p->v, d, p->seqlen, p->num_heads_kv, bdim, p->v_stride[2], p->v_stride[1],
+      !make_map(&m.v, p->v, f16, d, p->seqlen, p->num_heads_kv, bdim, p->v_stride[2], p->v_stride[1],
                 bstride(p->v_stride, p->num_heads_kv)))
     return BSFA_ERR_CUDA;
 
   DevParams dp{};
-  dp.o = static_cast<__nv_bfloat16*>(p->o);
+  dp.o = static_cast<uint16_t*>(p->o);
   dp.o_sb = varlen ? 0 : p->o_stride[0];
   dp.o_sh = p->o_stride[1];
   dp.o_st = p->o_stride[2];
@@ -395,7 +405,7 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   const int sms = num_sms();
   if (sms <= 0) return BSFA_ERR_CUDA;
   const int grid = (int)(units < sms ? units : sms);
-  if (dispatch<false>(d, nq, p->mode != BSFA_GATE_NONE, m, dp, grid, stream) != cudaSuccess)
+  if (dispatch<false>(f16, d, nq, p->mode != BSFA_GATE_NONE, m, dp, grid, stream) != cudaSuccess)
     return BSFA_ERR_CUDA;
   return BSFA_OK;
 }
@@ -407,7 +417,7 @@ size_t bsfa_calibrate_workspace_size(int Hq, int L, int Bq, int Bk) {
 }
 
 bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_samples,
-                           int n_samples, int Hq, int Hkv, int L, int d,
+                           int n_samples, int Hq, int Hkv, int L, int d, int dtype,
                            const int64_t q_stride[2], const int64_t k_stride[2], int Bq, int Bk,
                            float softmax_scale, const int* ks, int n_k, float* out,
                            void* workspace, size_t workspace_bytes, bsfa_stream_t stream_) {
@@ -415,6 +425,8 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
       !q_stride || !k_stride || !ks || n_k <= 0 || !out)
     return BSFA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return BSFA_ERR_UNSUPPORTED;
+  if (dtype != BSFA_DTYPE_BF16 && dtype != BSFA_DTYPE_F16) return BSFA_ERR_UNSUPPORTED;
+  const bool f16 = dtype == BSFA_DTYPE_F16;
   if ((Bq != 64 && Bq != 128) || (Bk != 64 && Bk != 128)) return BSFA_ERR_UNSUPPORTED;
   if (n_k > MAX_BUDGETS) return BSFA_ERR_UNSUPPORTED;
   for (int i = 0; i < n_k; ++i)
@@ -486,13 +498,13 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
 
   for (int n = 0; n < n_samples; ++n) {
     Maps m;
-    if (!make_map(&m.q, q_samples[n], d, L, Hq, 1, q_stride[1], q_stride[0],
+    if (!make_map(&m.q, q_samples[n], f16, d, L, Hq, 1, q_stride[1], q_stride[0],
                   (long long)q_stride[0] * Hq) ||
-        !make_map(&m.k, k_samples[n], d, L, Hkv, 1, k_stride[1], k_stride[0],
+        !make_map(&m.k, k_samples[n], f16, d, L, Hkv, 1, k_stride[1], k_stride[0],
                   (long long)k_stride[0] * Hkv))
       return BSFA_ERR_CUDA;
     m.v = m.k;
-    if (dispatch<true>(d, nq, true, m, dp, grid, stream) != cudaSuccess) return BSFA_ERR_CUDA;
+    if (dispatch<true>(f16, d, nq, true, m, dp, grid, stream) != cudaSuccess) return BSFA_ERR_CUDA;
     sa.sample = n;
     select_kernel<<<dim3(nqb, Hq), sel_threads, sel_smem, stream>>>(sa);
     if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;

@@ -51,7 +51,7 @@ enum : unsigned {
 };
 
 struct DevParams {
-  __nv_bfloat16* o;
+  uint16_t* o;                // bf16 or f16 elements (the kernel's element type)
   long long o_sb, o_sh, o_st;
   int Hq, Hkv, group, pairs;  // pairs = group / NQ
   int varlen;
@@ -222,7 +222,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
     umma_ts(d_tmem, p_tmem + kk * 8, dv + ((kk * 2048) >> 4), idesc, (kk > 0 || acc) ? 1u : 0u);
 }
 
-template <int D, int NQ, bool GATING, bool CALIB>
+template <int D, int NQ, bool GATING, bool CALIB, bool F16>
 __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     bsfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -418,8 +418,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     // The whole warp runs the loop and the waits; one elected lane (always
     // the same lane: all 32 are active) issues every MMA and commit, so each
     // commit tracks that lane's earlier MMAs.
-    constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t IDESC_QK = idesc_f32acc<F16>(128, 128, false, false);
+    constexpr uint32_t IDESC_PV = idesc_f32acc<F16>(128, D, false, true);
     uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
     bool ok = true;
     // Descriptors: one 64-bit base per operand buffer; a K-step adds its
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                   const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
                   const uint64_t pp = f2_pack(p0, p1);
                   lsum2 = f2_add(lsum2, pp);
-                  pk[e] = pack_bf16x2(p0, p1);
+                  pk[e] = pack_x2<F16>(p0, p1);
                 }
               } else {
 #pragma unroll
@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                   const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
                   const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
                   lsum2 = f2_add(lsum2, f2_pack(p0, p1));
-                  pk[e] = pack_bf16x2(p0, p1);
+                  pk[e] = pack_x2<F16>(p0, p1);
                 }
               }
               tmem_st32(tS + hf * 32, pk);
@@ -879,7 +879,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         if (!(ok = bar_red_and(bar_id, 128, okl))) break;
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.o + (long long)si.w * p.o_sb + (long long)h * p.o_sh +
+        uint16_t* orow = p.o + (long long)si.w * p.o_sb + (long long)h * p.o_sh +
                               (long long)(si.x + qpos) * p.o_st;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
@@ -891,8 +891,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              pw[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
-                                  __uint_as_float(orr[2 * e + 1]) * inv_l);
+              pw[e] = pack_x2<F16>(__uint_as_float(orr[2 * e]) * inv_l,
+                                   __uint_as_float(orr[2 * e + 1]) * inv_l);
             uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
 #pragma unroll
             for (int e = 0; e < 4; ++e) dst[e] = pk[e];

@@ -4,10 +4,10 @@
 
 namespace bsfa {
 
-template <int D, int NQ, bool GATING, bool CALIB>
+template <int D, int NQ, bool GATING, bool CALIB, bool F16>
 cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream) {
   using LY = Layout<D, NQ, CALIB>;
-  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB>;
+  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16>;
   static bool configured[64] = {};  // the attribute is per device; set once on each
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -33,5 +33,5 @@ cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t
 
 }  // namespace bsfa
 
-#define BSFA_INSTANTIATE(D, NQ, G, C) \
-  template cudaError_t bsfa::launch_fwd<D, NQ, G, C>(const Maps&, const DevParams&, int, cudaStream_t);
+#define BSFA_INSTANTIATE(D, NQ, G, C, F) \
+  template cudaError_t bsfa::launch_fwd<D, NQ, G, C, F>(const Maps&, const DevParams&, int, cudaStream_t);

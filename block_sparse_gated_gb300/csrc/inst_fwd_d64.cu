@@ -1,8 +1,12 @@
 // Attention kernels for head_dim 64 (gated and gate-compiled-out).
 #include "inst_fwd.cuh"
 namespace bsfa {
-BSFA_INSTANTIATE(64, 2, true, false)
-BSFA_INSTANTIATE(64, 1, true, false)
-BSFA_INSTANTIATE(64, 2, false, false)
-BSFA_INSTANTIATE(64, 1, false, false)
+BSFA_INSTANTIATE(64, 2, true, false, false)
+BSFA_INSTANTIATE(64, 2, true, false, true)
+BSFA_INSTANTIATE(64, 1, true, false, false)
+BSFA_INSTANTIATE(64, 1, true, false, true)
+BSFA_INSTANTIATE(64, 2, false, false, false)
+BSFA_INSTANTIATE(64, 2, false, false, true)
+BSFA_INSTANTIATE(64, 1, false, false, false)
+BSFA_INSTANTIATE(64, 1, false, false, true)
 }  // namespace bsfa

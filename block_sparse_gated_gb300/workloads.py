@@ -48,9 +48,9 @@ def gaussian(shape, seed: int, stream: int, device="cpu") -> torch.Tensor:
 
 @dataclass
 class LayerInputs:
-    q: torch.Tensor  # bf16 [Hq, L, d]
-    k: torch.Tensor  # bf16 [Hkv, L, d]
-    v: torch.Tensor | None  # bf16 [Hkv, L, d]
+    q: torch.Tensor  # bf16 or fp16 [Hq, L, d]
+    k: torch.Tensor  # [Hkv, L, d], same type
+    v: torch.Tensor | None  # [Hkv, L, d], same type
     needle_blocks: list = field(default_factory=list)  # per KV head
     skip_tier: torch.Tensor | None = None  # bool [Hkv, nk]
 
@@ -58,8 +58,10 @@ class LayerInputs:
 def layer_inputs(Hq: int, Hkv: int, L: int, d: int, seed: int, device="cpu", *,
                  with_v: bool = True, sink_tokens: int = 0, sink_scale: float = 4.0,
                  needles: int = 0, needle_scale: float = 4.0, block: int = 128,
-                 skip_rate: float = 0.0, skip_scale: float = 0.01) -> LayerInputs:
-    """One attention layer's Q/K/V for a single sequence of length L."""
+                 skip_rate: float = 0.0, skip_scale: float = 0.01,
+                 dtype: torch.dtype = torch.bfloat16) -> LayerInputs:
+    """One attention layer's Q/K/V for a single sequence of length L, drawn
+    in fp32 and rounded once to ``dtype`` (bf16 or fp16)."""
     if Hq % Hkv:
         raise ValueError("Hq must be a multiple of Hkv")
     q = gaussian((Hq, L, d), seed, _STREAM_Q, device)
@@ -91,8 +93,7 @@ def layer_inputs(Hq: int, Hkv: int, L: int, d: int, seed: int, device="cpu", *,
         scale = torch.where(skip_tier, torch.tensor(skip_scale), torch.tensor(1.0))
         scale_tok = scale.repeat_interleave(block, dim=1)[:, :L].to(device)
         k *= scale_tok[:, :, None]
-    bf = torch.bfloat16
-    return LayerInputs(q.to(bf), k.to(bf), v.to(bf) if v is not None else None,
+    return LayerInputs(q.to(dtype), k.to(dtype), v.to(dtype) if v is not None else None,
                        needle_blocks, skip_tier)
 
 

@@ -71,9 +71,17 @@ typedef enum {
                               (the zero-skip overhead reference) */
 } bsfa_gate_mode;
 
+/* Element type of Q, K, V and O (one type for all four).  The tensor-core
+ * products accumulate in fp32 for either; P is rounded to this type before
+ * the PV product and O is rounded to it once, at the end. */
+typedef enum {
+  BSFA_DTYPE_BF16 = 0,
+  BSFA_DTYPE_F16 = 1
+} bsfa_dtype;
+
 /*
- * Parameters of one prefill call.  Q, K, V, O are bf16 with the head
- * dimension contiguous; every other dimension is addressed through strides
+ * Parameters of one prefill call.  Q, K, V, O share one 16-bit element type
+ * (`dtype`: bf16 or fp16) with the head dimension contiguous; every other dimension is addressed through strides
  * given in ELEMENTS as {batch, head, token}.  Two layouts are accepted:
  *   - batched  (cu_seqlens == NULL): `batch` sequences of `seqlen` tokens,
  *     e.g. [B, H, L, d] or [B, L, H, d];
@@ -84,10 +92,10 @@ typedef enum {
  * 16-byte aligned (TMA requirement).  q-head h reads KV head h / (Hq/Hkv).
  */
 typedef struct {
-  const void* q;              /* bf16 [.., Hq, .., d]  */
-  const void* k;              /* bf16 [.., Hkv, .., d] */
-  const void* v;              /* bf16 [.., Hkv, .., d] */
-  void* o;                    /* bf16, same shape as q; rows past a sequence end untouched */
+  const void* q;              /* [.., Hq, .., d]  */
+  const void* k;              /* [.., Hkv, .., d] */
+  const void* v;              /* [.., Hkv, .., d] */
+  void* o;                    /* same shape as q; rows past a sequence end untouched */
   int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3]; /* {batch, head, token} */
   int batch;                  /* number of sequences (>= 0; 0 is a no-op) */
   int num_heads_q;            /* Hq */
@@ -117,6 +125,8 @@ typedef struct {
   void* workspace;            /* device scratch, >= bsfa_prefill_workspace_size bytes,
                                  256-byte aligned; its contents are not preserved */
   size_t workspace_bytes;
+  int dtype;                  /* bsfa_dtype of q, k, v and o; 0 (a zeroed struct) is bf16;
+                                 any other value is BSFA_ERR_UNSUPPORTED */
 } bsfa_fwd_params;
 
 /* Bytes of workspace bsfa_prefill_fwd needs for these parameters (reads the
@@ -174,8 +184,8 @@ bsfa_status bsfa_prefill_fwd_noalloc(const bsfa_fwd_params* p, bsfa_stream_t str
 
 /*
  * Offline threshold calibration for one layer and a set of budgets.
- *   q_samples / k_samples: HOST arrays of n_samples DEVICE pointers to bf16
- *     tensors of one sample each, layout [H, L, d] addressed by the strides
+ *   q_samples / k_samples: HOST arrays of n_samples DEVICE pointers to
+ *     tensors (element type `dtype`, a bsfa_dtype) of one sample each, layout [H, L, d] addressed by the strides
  *     {head, token} in elements (d contiguous), equal L for every sample.
  *   ks: HOST array of n_k budgets (each >= 1).
  *   thresholds_out: device fp32 [n_k][Hq][ceil(L/Bq)], overwritten with the
@@ -188,7 +198,8 @@ size_t bsfa_calibrate_workspace_size(int num_heads_q, int seqlen, int block_q, i
 
 bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_samples,
                            int n_samples, int num_heads_q, int num_heads_kv, int seqlen,
-                           int head_dim, const int64_t q_stride[2], const int64_t k_stride[2],
+                           int head_dim, int dtype,
+                           const int64_t q_stride[2], const int64_t k_stride[2],
                            int block_q, int block_k, float softmax_scale,
                            const int* ks, int n_k, float* thresholds_out,
                            void* workspace, size_t workspace_bytes, bsfa_stream_t stream);

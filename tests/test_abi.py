@@ -66,7 +66,11 @@ def test_host_side_validation_without_gpu(libpath):
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unsupported head_dim
     p.head_dim, p.block_k = 128, 96
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unsupported block size
-    p.block_k = 128
+    p.block_k, p.dtype = 128, 7
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unknown element type
+    p.dtype = _native.DTYPE_F16
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # null tensors
+    p.dtype = _native.DTYPE_BF16
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # null tensors
     p.batch = 0
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 0  # empty batch is a no-op
@@ -74,3 +78,40 @@ def test_host_side_validation_without_gpu(libpath):
     assert L.bsfa_prefill_workspace_size(ctypes.byref(p)) > 0
     w = ctypes.c_int(0)
     assert L.bsfa_bitmap_words_per_row(ctypes.byref(p), ctypes.byref(w)) == 0 and w.value == 1
+
+
+def test_params_struct_layout_matches_header(libpath):
+    """The ctypes mirror ends with the same field the header's struct ends
+    with, at the C compiler's offset (checked by compiling a tiny probe)."""
+    import ctypes
+    import tempfile
+    from block_sparse_gated_gb300 import _native
+    src = (
+        '#include <stddef.h>\n#include <stdio.h>\n#include "bsfa.h"\n'
+        'int main(void) { printf("%zu %zu %zu\\n", sizeof(bsfa_fwd_params), '
+        'offsetof(bsfa_fwd_params, workspace_bytes), offsetof(bsfa_fwd_params, dtype)); '
+        'return 0; }\n')
+    with tempfile.TemporaryDirectory() as tmp:
+        c = os.path.join(tmp, "probe.c")
+        exe = os.path.join(tmp, "probe")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        size, off_ws, off_dt = map(int, subprocess.run([exe], capture_output=True, text=True,
+                                                         check=True).stdout.split())
+    F = _native.FwdParams
+    assert (ctypes.sizeof(F), F.workspace_bytes.offset, F.dtype.offset) == (size, off_ws, off_dt)
+
+
+def test_mixed_element_types_are_rejected_before_the_library():
+    import torch
+    from block_sparse_gated_gb300 import api
+    q = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 128, 64, dtype=torch.float16)
+    with pytest.raises(TypeError):
+        api._params(q, k, k, q, layout=None, cu_seqlens=None, max_seqlen=None, block_q=128,
+                    block_k=128, softmax_scale=None, mode="none", thresholds=None,
+                    log_lambda=None)
+    with pytest.raises(TypeError):
+        api._params(q.float(), q.float(), q.float(), q.float(), layout=None, cu_seqlens=None,
+                    max_seqlen=None, block_q=128, block_k=128, softmax_scale=None, mode="none",
+                    thresholds=None, log_lambda=None)

@@ -350,7 +350,8 @@ def e2e(q, k, v, slices, flops, Bq, Bk, args, dev):
 
 def lambda_sweep(dev, args):
     """lambda gate at 64K: time vs dialled skip rate, plus the same kernel with
-    the gate compiled out (0-skip overhead)."""
+    the gate compiled out (0-skip overhead), and the A/B against loading V for
+    skipped tiles too (``v_always``: same results, V read for every tile)."""
     import torch
 
     import block_sparse_gated_gb300 as bsfa
@@ -386,7 +387,10 @@ def lambda_sweep(dev, args):
         row = {"target_skip": r, "log_lambda": ll if math.isfinite(ll) else "-inf",
                "measured_skip": round(1 - kc / cand, 4), "ms": round(ms, 3),
                "effective_tflops": round(effective_flops((kc, cand, diag), B, B, d) /
-                                         (ms * 1e-3) / 1e12, 1)}
+                                         (ms * 1e-3) / 1e12, 1),
+               "ms_v_always": round(timed(lambda: bsfa.prefill(
+                   q, k, v, mode="lambda", log_lambda=ll, out=out, workspace=ws,
+                   v_always=True)), 3)}
         if r == 0:
             thr = torch.full((Hq, 1), -math.inf, device=dev)
             row["ms_threshold_minus_inf"] = round(timed(lambda: bsfa.prefill(
@@ -400,7 +404,8 @@ def lambda_sweep(dev, args):
     return {"workload": "lambda-sweep-L65536", "rows": rows,
             "zero_skip_overhead_lambda": round(rows[0]["ms"] / base - 1, 4),
             "zero_skip_overhead_threshold": round(rows[0]["ms_threshold_minus_inf"] / base - 1, 4),
-            "monotonic": all(a > b for a, b in zip(times, times[1:]))}
+            "monotonic": all(a > b for a, b in zip(times, times[1:])),
+            "v_always_over_gated_v": [round(r_["ms_v_always"] / r_["ms"], 4) for r_ in rows]}
 
 
 def _timed(fn, reps):

@@ -30,12 +30,14 @@ class FwdParams(ctypes.Structure):
         ("log_lambda", c_float),
         ("kept_bitmap", c_void_p), ("lse", c_void_p), ("block_counts", c_void_p),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
-        ("dtype", c_int),
+        ("dtype", c_int), ("flags", ctypes.c_uint),
     ]
 
 
 # bsfa_dtype
 DTYPE_BF16, DTYPE_F16 = 0, 1
+# bsfa_flag
+FLAG_V_ALWAYS = 1
 
 
 # Every exported symbol and its C signature: (name, restype, argtypes).

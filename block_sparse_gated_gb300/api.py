@@ -73,7 +73,7 @@ def _strides_bhtd(t: torch.Tensor, layout: str, varlen: bool):
 
 
 def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, softmax_scale,
-            mode, thresholds, log_lambda):
+            mode, thresholds, log_lambda, v_always=False):
     varlen = cu_seqlens is not None
     if layout is None:
         layout = "htd" if varlen else "bhld"
@@ -109,6 +109,7 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
         p.thresholds, p.thresholds_nq = None, 0
     p.log_lambda = float(log_lambda) if log_lambda is not None else 0.0
     p.dtype = _dtype_code(q)
+    p.flags = _native.FLAG_V_ALWAYS if v_always else 0
     return p
 
 
@@ -124,18 +125,19 @@ def bitmap_shape(num_heads_q: int, *, block_q: int, block_k: int, seqlens) -> tu
 def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="threshold",
             thresholds=None, log_lambda=None, cu_seqlens=None, max_seqlen=None, layout=None,
             out=None, return_bitmap=False, return_lse=False, return_counts=False,
-            workspace=None, stream=None):
+            workspace=None, stream=None, v_always=False):
     """Gated causal prefill.  Batched: q [B, Hq, L, d] (layout "bhld") or
     [B, L, Hq, d] ("blhd"); varlen (cu_seqlens int32 on the device): q [Hq, T, d]
     ("htd") or [T, Hq, d] ("thd").  Returns a dict with "out" and, on request,
     "bitmap" (int32 [rows, Hq, words], bit j of word j//32 = keep), "lse"
     (float32 [Hq, rows_of_tokens]) and "counts" (int64 [3]: kept candidates,
-    candidates, diagonal-region blocks)."""
+    candidates, diagonal-region blocks).  ``v_always`` loads V for skipped
+    tiles too (results unchanged; for measuring what the skipped load saves)."""
     if out is None:
         out = torch.empty_like(q)
     p = _params(q, k, v, out, layout=layout, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
                 block_q=block_q, block_k=block_k, softmax_scale=softmax_scale, mode=mode,
-                thresholds=thresholds, log_lambda=log_lambda)
+                thresholds=thresholds, log_lambda=log_lambda, v_always=v_always)
     L = _native.lib()
     res = {"out": out}
     dev = q.device

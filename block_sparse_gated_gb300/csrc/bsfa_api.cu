@@ -201,31 +201,37 @@ static unsigned* error_word() {
 }
 
 template <bool CALIB, bool F16>
-static cudaError_t dispatch_t(int d, int nq, bool gating, const Maps& m, const DevParams& p,
-                            int grid, cudaStream_t st) {
+static cudaError_t dispatch_t(int d, int nq, bool gating, bool vall, const Maps& m,
+                              const DevParams& p, int grid, cudaStream_t st) {
   if (CALIB) {
-    if (d == 128) return nq == 2 ? launch_fwd<128, 2, true, true, F16>(m, p, grid, st)
-                                 : launch_fwd<128, 1, true, true, F16>(m, p, grid, st);
-    return nq == 2 ? launch_fwd<64, 2, true, true, F16>(m, p, grid, st)
-                   : launch_fwd<64, 1, true, true, F16>(m, p, grid, st);
+    if (d == 128) return nq == 2 ? launch_fwd<128, 2, true, true, F16, false>(m, p, grid, st)
+                                 : launch_fwd<128, 1, true, true, F16, false>(m, p, grid, st);
+    return nq == 2 ? launch_fwd<64, 2, true, true, F16, false>(m, p, grid, st)
+                   : launch_fwd<64, 1, true, true, F16, false>(m, p, grid, st);
+  }
+  if (gating && vall) {
+    if (d == 128) return nq == 2 ? launch_fwd<128, 2, true, false, F16, true>(m, p, grid, st)
+                                 : launch_fwd<128, 1, true, false, F16, true>(m, p, grid, st);
+    return nq == 2 ? launch_fwd<64, 2, true, false, F16, true>(m, p, grid, st)
+                   : launch_fwd<64, 1, true, false, F16, true>(m, p, grid, st);
   }
   if (d == 128) {
-    if (gating) return nq == 2 ? launch_fwd<128, 2, true, false, F16>(m, p, grid, st)
-                               : launch_fwd<128, 1, true, false, F16>(m, p, grid, st);
-    return nq == 2 ? launch_fwd<128, 2, false, false, F16>(m, p, grid, st)
-                   : launch_fwd<128, 1, false, false, F16>(m, p, grid, st);
+    if (gating) return nq == 2 ? launch_fwd<128, 2, true, false, F16, false>(m, p, grid, st)
+                               : launch_fwd<128, 1, true, false, F16, false>(m, p, grid, st);
+    return nq == 2 ? launch_fwd<128, 2, false, false, F16, false>(m, p, grid, st)
+                   : launch_fwd<128, 1, false, false, F16, false>(m, p, grid, st);
   }
-  if (gating) return nq == 2 ? launch_fwd<64, 2, true, false, F16>(m, p, grid, st)
-                             : launch_fwd<64, 1, true, false, F16>(m, p, grid, st);
-  return nq == 2 ? launch_fwd<64, 2, false, false, F16>(m, p, grid, st)
-                 : launch_fwd<64, 1, false, false, F16>(m, p, grid, st);
+  if (gating) return nq == 2 ? launch_fwd<64, 2, true, false, F16, false>(m, p, grid, st)
+                             : launch_fwd<64, 1, true, false, F16, false>(m, p, grid, st);
+  return nq == 2 ? launch_fwd<64, 2, false, false, F16, false>(m, p, grid, st)
+                 : launch_fwd<64, 1, false, false, F16, false>(m, p, grid, st);
 }
 
 template <bool CALIB>
-static cudaError_t dispatch(bool f16, int d, int nq, bool gating, const Maps& m,
+static cudaError_t dispatch(bool f16, int d, int nq, bool gating, bool vall, const Maps& m,
                             const DevParams& p, int grid, cudaStream_t st) {
-  return f16 ? dispatch_t<CALIB, true>(d, nq, gating, m, p, grid, st)
-             : dispatch_t<CALIB, false>(d, nq, gating, m, p, grid, st);
+  return f16 ? dispatch_t<CALIB, true>(d, nq, gating, vall, m, p, grid, st)
+             : dispatch_t<CALIB, false>(d, nq, gating, vall, m, p, grid, st);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -272,6 +278,7 @@ static bsfa_status validate(const bsfa_fwd_params* p) {
     return BSFA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return BSFA_ERR_UNSUPPORTED;
   if (p->dtype != BSFA_DTYPE_BF16 && p->dtype != BSFA_DTYPE_F16) return BSFA_ERR_UNSUPPORTED;
+  if (p->flags & ~static_cast<unsigned>(BSFA_FLAG_V_ALWAYS)) return BSFA_ERR_UNSUPPORTED;
   if ((p->block_q != 64 && p->block_q != 128) || (p->block_k != 64 && p->block_k != 128))
     return BSFA_ERR_UNSUPPORTED;
   if (p->mode < BSFA_GATE_THRESHOLD || p->mode > BSFA_GATE_NONE) return BSFA_ERR_INVALID_ARG;
@@ -405,7 +412,8 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   const int sms = num_sms();
   if (sms <= 0) return BSFA_ERR_CUDA;
   const int grid = (int)(units < sms ? units : sms);
-  if (dispatch<false>(f16, d, nq, p->mode != BSFA_GATE_NONE, m, dp, grid, stream) != cudaSuccess)
+  const bool vall = (p->flags & BSFA_FLAG_V_ALWAYS) != 0;
+  if (dispatch<false>(f16, d, nq, p->mode != BSFA_GATE_NONE, vall, m, dp, grid, stream) != cudaSuccess)
     return BSFA_ERR_CUDA;
   return BSFA_OK;
 }
@@ -504,7 +512,7 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
                   (long long)k_stride[0] * Hkv))
       return BSFA_ERR_CUDA;
     m.v = m.k;
-    if (dispatch<true>(f16, d, nq, true, m, dp, grid, stream) != cudaSuccess) return BSFA_ERR_CUDA;
+    if (dispatch<true>(f16, d, nq, true, false, m, dp, grid, stream) != cudaSuccess) return BSFA_ERR_CUDA;
     sa.sample = n;
     select_kernel<<<dim3(nqb, Hq), sel_threads, sel_smem, stream>>>(sa);
     if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;

@@ -222,7 +222,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
     umma_ts(d_tmem, p_tmem + kk * 8, dv + ((kk * 2048) >> 4), idesc, (kk > 0 || acc) ? 1u : 0u);
 }
 
-template <int D, int NQ, bool GATING, bool CALIB, bool F16>
+// VALL (gated only): load V for every visible tile, kept or not.
+template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL>
 __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     bsfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -381,13 +382,17 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       for (int J = 0; J < nkt; ++J, ++tc) {
         // Every slot's decision is read on every tile (V is issued on the
         // first one that keeps the tile), so this warp consumes each
-        // decision phase in order instead of skipping some.
-        bool need = false, issued = false;
+        // decision phase in order instead of skipping some.  With VALL no
+        // decision is read: V of every tile is issued as early as a stage
+        // is free, like the gate-compiled-out producer does.
+        bool need = VALL, issued = false;
         for (int s = 0; s < NQ && ok; ++s) {
-          if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
-                              ERR_WAIT_DEC)))
-            break;
-          need = need || c->dec[s][tc & 1] != 0u;
+          if constexpr (!VALL) {
+            if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
+                                ERR_WAIT_DEC)))
+              break;
+            need = need || c->dec[s][tc & 1] != 0u;
+          }
           if (!need || issued) continue;
           issued = true;
           const uint32_t st = vc % VST;
@@ -520,6 +525,14 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
           if (do_qk && s == NQ - 1) ++kc;
         }
         if (!ok) break;
+        if constexpr (GATING && !CALIB && VALL) {
+          // This tile's V was loaded whether or not a slot kept it.
+          if (!vready) {
+            if (!(ok = wait_all(&c->v_full[vst], (vc / VST) & 1, abort, p.err, ERR_WAIT_V_FULL)))
+              break;
+            any = true;
+          }
+        }
         if (!CALIB && any) {
           if (elect_one()) umma_commit(&c->v_empty[vst]);
           __syncwarp();

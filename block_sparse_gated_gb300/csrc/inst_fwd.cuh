@@ -4,10 +4,10 @@
 
 namespace bsfa {
 
-template <int D, int NQ, bool GATING, bool CALIB, bool F16>
+template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL>
 cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream) {
   using LY = Layout<D, NQ, CALIB>;
-  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16>;
+  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL>;
   static bool configured[64] = {};  // the attribute is per device; set once on each
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -33,5 +33,6 @@ cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t
 
 }  // namespace bsfa
 
-#define BSFA_INSTANTIATE(D, NQ, G, C, F) \
-  template cudaError_t bsfa::launch_fwd<D, NQ, G, C, F>(const Maps&, const DevParams&, int, cudaStream_t);
+#define BSFA_INSTANTIATE(D, NQ, G, C, F) BSFA_INSTANTIATE_V(D, NQ, G, C, F, false)
+#define BSFA_INSTANTIATE_V(D, NQ, G, C, F, VA) \
+  template cudaError_t bsfa::launch_fwd<D, NQ, G, C, F, VA>(const Maps&, const DevParams&, int, cudaStream_t);

@@ -79,6 +79,16 @@ typedef enum {
   BSFA_DTYPE_F16 = 1
 } bsfa_dtype;
 
+/* Bits of bsfa_fwd_params.flags. */
+typedef enum {
+  /* THRESHOLD and LAMBDA modes: load the V tile of every visible key tile,
+   * kept or not, ahead of the gate (as the BLASST SM100 kernel does, "V is
+   * still loaded" in its discussion of skipped blocks); skipped tiles still
+   * get no exp, no P.V and no m/l/O update, so results are bit-identical to
+   * flags = 0.  Exists to measure what skipping the V load saves. */
+  BSFA_FLAG_V_ALWAYS = 1
+} bsfa_flag;
+
 /*
  * Parameters of one prefill call.  Q, K, V, O share one 16-bit element type
  * (`dtype`: bf16 or fp16) with the head dimension contiguous; every other dimension is addressed through strides
@@ -127,6 +137,8 @@ typedef struct {
   size_t workspace_bytes;
   int dtype;                  /* bsfa_dtype of q, k, v and o; 0 (a zeroed struct) is bf16;
                                  any other value is BSFA_ERR_UNSUPPORTED */
+  unsigned int flags;         /* bsfa_flag bits (0 = default); unknown bits are
+                                 BSFA_ERR_UNSUPPORTED */
 } bsfa_fwd_params;
 
 /* Bytes of workspace bsfa_prefill_fwd needs for these parameters (reads the

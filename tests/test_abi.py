@@ -68,8 +68,11 @@ def test_host_side_validation_without_gpu(libpath):
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unsupported block size
     p.block_k, p.dtype = 128, 7
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unknown element type
-    p.dtype = _native.DTYPE_F16
+    p.dtype, p.flags = _native.DTYPE_F16, 2
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unknown flag bit
+    p.flags = _native.FLAG_V_ALWAYS
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # null tensors
+    p.flags = 0
     p.dtype = _native.DTYPE_BF16
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # null tensors
     p.batch = 0
@@ -89,17 +92,17 @@ def test_params_struct_layout_matches_header(libpath):
     src = (
         '#include <stddef.h>\n#include <stdio.h>\n#include "bsfa.h"\n'
         'int main(void) { printf("%zu %zu %zu\\n", sizeof(bsfa_fwd_params), '
-        'offsetof(bsfa_fwd_params, workspace_bytes), offsetof(bsfa_fwd_params, dtype)); '
+        'offsetof(bsfa_fwd_params, dtype), offsetof(bsfa_fwd_params, flags)); '
         'return 0; }\n')
     with tempfile.TemporaryDirectory() as tmp:
         c = os.path.join(tmp, "probe.c")
         exe = os.path.join(tmp, "probe")
         open(c, "w").write(src)
         subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
-        size, off_ws, off_dt = map(int, subprocess.run([exe], capture_output=True, text=True,
+        size, off_dt, off_fl = map(int, subprocess.run([exe], capture_output=True, text=True,
                                                          check=True).stdout.split())
     F = _native.FwdParams
-    assert (ctypes.sizeof(F), F.workspace_bytes.offset, F.dtype.offset) == (size, off_ws, off_dt)
+    assert (ctypes.sizeof(F), F.dtype.offset, F.flags.offset) == (size, off_dt, off_fl)
 
 
 def test_mixed_element_types_are_rejected_before_the_library():

@@ -267,3 +267,27 @@ def test_soak_back_to_back_launches(cuda_device):
     for o in outs:
         assert torch.equal(o["out"], first["out"])
         assert torch.equal(o["bitmap"], first["bitmap"])
+
+
+# ------------------------------------------------------- V loaded for every tile
+@pytest.mark.parametrize("mode", ["threshold", "lambda"])
+@pytest.mark.parametrize("Bq,Bk,d", [(128, 128, 128), (64, 64, 64)])
+def test_v_always_is_bit_identical(cuda_device, mode, Bq, Bk, d):
+    """Loading V for skipped tiles too (the flag that exists for the A/B
+    against skipping the load) changes no output bit; the case does skip
+    blocks."""
+    Hq, Hkv, L = 4, 2, 1500
+    x, q, k, v = _inputs(Hq, Hkv, L, d, 91, cuda_device, skip_rate=0.6, needles=2, block=Bk)
+    kw = dict(block_q=Bq, block_k=Bk, mode=mode)
+    if mode == "lambda":
+        kw["log_lambda"] = -1.0
+    else:
+        table = gu.median_table(gu.to64(x.q), gu.to64(x.k), Bq, Bk, gu.default_sigma(d))
+        kw["thresholds"] = torch.from_numpy(table.astype(np.float32)).to(cuda_device)
+    a = _run(q, k, v, **kw)
+    b = _run(q, k, v, v_always=True, **kw)
+    assert torch.equal(a["out"], b["out"])
+    assert torch.equal(a["bitmap"], b["bitmap"])
+    assert torch.equal(a["lse"], b["lse"])
+    kept, cand = a["counts"].cpu().tolist()[:2]
+    assert 0 < kept < cand

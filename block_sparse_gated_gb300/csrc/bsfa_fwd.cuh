@@ -34,7 +34,12 @@ constexpr int TILE = 128;
 constexpr int KST = 2;  // K ring stages
 constexpr int VST = 2;  // V ring stages
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
-constexpr float RESCALE_LOG2 = 8.0f;  // lazy rescale: P may grow to 2^8 before O is rescaled
+constexpr float RESCALE_LOG2 = 8.0f;
+// Decision words carry the tile counter above the four decision bits, so a
+// reader can tell a published decision from the word of two tiles earlier.
+constexpr uint32_t DEC_BITS = 4;
+constexpr uint32_t DEC_MASK = (1u << DEC_BITS) - 1u;
+constexpr uint32_t DEC_STAMP_MASK = 0x0FFFFFFFu;  // lazy rescale: P may grow to 2^8 before O is rescaled
 // Register split for two slots (384 threads): warpgroup 0 (copies, MMA issue)
 // drops to COPY_REGS, the two softmax warpgroups rise to SOFTMAX_REGS.  The
 // host checks 128*COPY_REGS + 256*SOFTMAX_REGS against the registers the
@@ -46,7 +51,7 @@ constexpr int SOFTMAX_REGS = 200;
 enum : unsigned {
   ERR_WAIT_Q_EMPTY = 0x101, ERR_WAIT_K_EMPTY, ERR_WAIT_V_EMPTY, ERR_WAIT_DEC,
   ERR_WAIT_Q_FULL, ERR_WAIT_K_FULL, ERR_WAIT_V_FULL, ERR_WAIT_P_FULL, ERR_WAIT_O_EMPTY,
-  ERR_WAIT_S_FULL, ERR_WAIT_WG, ERR_WAIT_O_FULL, ERR_WAIT_DRAIN,
+  ERR_WAIT_S_FULL, ERR_WAIT_WG, ERR_WAIT_O_FULL, ERR_WAIT_DRAIN, ERR_WAIT_RED,
   ERR_WAIT_SELFTEST = 0x1FF
 };
 
@@ -81,7 +86,12 @@ struct Ctrl {
   uint64_t q_empty;
   uint64_t k_full[KST], k_empty[KST];
   uint64_t v_full[VST], v_empty[VST];
-  uint64_t s_full[NQ], p_full[NQ], o_full[NQ], o_empty[NQ];
+  uint64_t s_full[NQ], o_full[NQ], o_empty[NQ];
+  // Per tile parity: P written (or the tile skipped) by all 128 threads of a
+  // slot; calibration maxima of a slot's four warps in (128 arrivals); the
+  // decision word published by the slot's first warp (32 arrivals).
+  uint64_t p_full[NQ][2];
+  uint64_t red_full[NQ][2];
   uint64_t dec_full[NQ][2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -248,11 +258,13 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     for (int s = 0; s < NQ; ++s) {
       mbar_init(&c->q_full[s], 1);
       mbar_init(&c->s_full[s], 1);
-      mbar_init(&c->p_full[s], 128);
       mbar_init(&c->o_full[s], 1);
       mbar_init(&c->o_empty[s], 128);
-      mbar_init(&c->dec_full[s][0], 32);
-      mbar_init(&c->dec_full[s][1], 32);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&c->p_full[s][b], 128);
+        mbar_init(&c->red_full[s][b], 128);
+        mbar_init(&c->dec_full[s][b], 32);
+      }
     }
     mbar_init(&c->q_empty, 1);
     for (int i = 0; i < KST; ++i) {
@@ -264,6 +276,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       mbar_init(&c->v_empty[i], 1);
     }
     mbar_init(&c->drain, 1);
+    for (int s = 0; s < NQ; ++s) c->dec[s][0] = c->dec[s][1] = 0xFFFFFFFFu;  // no stamp matches
     c->abort = 0;
     fence_mbarrier_init();
   }
@@ -391,7 +404,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
                                 ERR_WAIT_DEC)))
               break;
-            need = need || c->dec[s][tc & 1] != 0u;
+            need = need || (c->dec[s][tc & 1] & DEC_MASK) != 0u;
           }
           if (!need || issued) continue;
           issued = true;
@@ -462,14 +475,28 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         for (int s = 0; s < NQ; ++s) {
           bool do_pv = false;
           uint32_t acc = 1u;
+          const bool do_qk = J + 1 < nkt;
+          const uint32_t ppar = (tc >> 1) & 1u;
+          // Every shared-memory access of this warp queues behind the
+          // operand reads of the MMAs it has just issued (Q.K^T reads both
+          // operands from shared memory at the full shared-memory rate), so
+          // one access costs hundreds of cycles.  Probe everything this step
+          // may need -- the decision word, V, P and the next K tile -- back
+          // to back without blocking (one round trip for all of them), and
+          // block only on what was not ready.
+          const bool v_ok = CALIB || vready || mbar_test_wait(&c->v_full[vst], (vc / VST) & 1);
+          const bool p_ok = mbar_test_wait(&c->p_full[s][tb], ppar);
+          const bool k_ok = !(do_qk && s == 0) || mbar_test_wait(&c->k_full[kst], (kc / KST) & 1);
+          const uint32_t dw = (GATING && !CALIB) ? ld_acquire_u32(&c->dec[s][tb]) : 0u;
           if constexpr (!CALIB) {
-            // The decision is published after pass 1, well before P: read it
-            // (and wait for V and O) while the softmax is still writing P.
             uint32_t dec = 1u;
             if constexpr (GATING) {
-              if (!(ok = wait_all(&c->dec_full[s][tb], (tc >> 1) & 1, abort, p.err, ERR_WAIT_DEC)))
-                break;
-              dec = c->dec[s][tb];
+              uint32_t w = dw;
+              if ((w >> DEC_BITS) != (tc & DEC_STAMP_MASK)) {  // not published yet
+                if (!(ok = wait_all(&c->dec_full[s][tb], ppar, abort, p.err, ERR_WAIT_DEC))) break;
+                w = ld_acquire_u32(&c->dec[s][tb]);
+              }
+              dec = w & DEC_MASK;
             }
             if (dec != 0u) {
               any = true;
@@ -477,8 +504,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
               if (!vready) {
                 // V arrives by TMA into shared memory: the mbarrier completion
                 // orders it before the MMA (no TMEM hand-off, no tcgen05 fence).
-                if (!(ok = wait_all(&c->v_full[vst], (vc / VST) & 1, abort, p.err,
-                                    ERR_WAIT_V_FULL)))
+                if (!v_ok && !(ok = wait_all(&c->v_full[vst], (vc / VST) & 1, abort, p.err,
+                                             ERR_WAIT_V_FULL)))
                   break;
                 vready = true;
               }
@@ -486,27 +513,29 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                 if (!(ok = wait_all(&c->o_empty[s], (uc & 1) ^ 1, abort, p.err,
                                     ERR_WAIT_O_EMPTY)))
                   break;
-                tc_fence_after();
                 acc = 0u;
                 first_mask &= ~(1u << s);
               }
             }
           }
           // A skipped tile has no P: its S was read before the decision was
-          // published, so the next S may be issued now.  (The next decision
-          // is published only after every thread has arrived on p_full for
-          // this tile, so this phase completes before the next wait on it.)
-          if (CALIB || !GATING || do_pv) {
-            if (!(ok = wait_all(&c->p_full[s], tc & 1, abort, p.err, ERR_WAIT_P_FULL))) break;
+          // published, so the next S may be issued now.  The P barrier of
+          // this tile parity is then not waited on: its previous phase (tile
+          // tc - 2) completed before this tile's S was issued (that issue
+          // followed either the P of tile tc - 1, or a skip decision, which
+          // is published only after the vote barrier of tile tc - 1, which
+          // each thread reaches after its arrival for tile tc - 2), so a
+          // later wait on it never falls two phases behind.
+          if ((CALIB || !GATING || do_pv) && !p_ok) {
+            if (!(ok = wait_all(&c->p_full[s][tb], ppar, abort, p.err, ERR_WAIT_P_FULL))) break;
           }
           tc_fence_after();
-          const bool do_qk = J + 1 < nkt;
           // P.V for this tile first: it does not need the next K tile.
           if (do_pv && elect_one())
             issue_pv<D, NQ>(tmem + NQ * 128 + s * D, tmem + s * 128, dV + ((vst * TB) >> 4),
                             IDESC_PV, acc);
           __syncwarp();
-          if (do_qk && s == 0) {
+          if (do_qk && s == 0 && !k_ok) {
             if (!(ok = wait_all(&c->k_full[kst], (kc / KST) & 1, abort, p.err, ERR_WAIT_K_FULL)))
               break;
           }
@@ -558,7 +587,6 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     const int s = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const uint32_t bar_id = 1 + s;  // named barrier of this warpgroup
     const uint32_t tlane = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + tlane + s * 128;
     const uint32_t tO = tmem + tlane + NQ * 128 + s * D;
@@ -571,6 +599,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     // splits the warp (a one-lane branch here slowed the whole warp's
     // exp pass); lane 0 alone stores.
     const bool lead_warp = ((wq * 32) % p.Bq) == 0;
+    const uint32_t bar_id = 1 + s;  // named barrier of this warpgroup (gated kernel)
     const float sc = p.sigma_log2;
     uint32_t tc = 0, uc = 0;
     bool ok = true;
@@ -601,7 +630,20 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 
       for (int J = 0; J < nkt; ++J, ++tc) {
         const int tb = tc & 1;
-        const bool okl = wait_bar(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL);
+        const uint32_t ph = (tc >> 1) & 1u;  // phase parity of the per-tile-parity barriers
+        // Waits here are bounded.  In the gated kernel every thread joins the
+        // per-tile vote barrier even after its own wait gave up, and the
+        // barrier's count tells all of them, so the warpgroup leaves together
+        // (its named barriers can never strand a warp).  The other kernels use
+        // no named barrier in this loop: a warp that gives up leaves alone and
+        // the others' bounded waits see the abort flag.
+        bool okl;
+        if constexpr (GATING && !CALIB) {
+          okl = wait_bar(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL);
+        } else {
+          if (!(ok = wait_all(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL))) break;
+          okl = true;
+        }
         tc_fence_after();
         const bool diag_tile = (J == I);  // keys beyond a row exist only in the last tile
 
@@ -657,66 +699,34 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         // some row's maximum does (scaling by sigma > 0 is monotone in fp32),
         // so the OR of the row votes equals comparing s_max(i,j) with T.
         // Lambda: row r wants the first sub-block when
-        // sigma * (rowmax_r - m_r) >= ln(lambda).  One barrier per tile also
-        // settles whether every thread of the warpgroup is still running.
+        // sigma * (rowmax_r - m_r) >= ln(lambda).
         const bool lambda_mode = GATING && !CALIB && p.mode == 1;
-        // One 128x128 semantic block per tile: the barrier itself carries the
-        // vote.  Lane 0 of each warp counts 1 when some lane of the warp has
-        // stopped, lanes 1..8 count 1 each when some row of the warp wants the
-        // block, so the count is F + 8 V with F, V <= 4.
-        bool tile_vote = false;
         if constexpr (CALIB) {
           const float w0 = warp_max_f32(rvalid ? rm0 : -CUDART_INF_F);
           const float w1 = (KS == 1) ? w0 : warp_max_f32(rvalid ? rm1 : -CUDART_INF_F);
           c->red[s][tb][wq][0] = w0;  // every lane: same value
           c->red[s][tb][wq][1] = w1;
-        } else if constexpr (GATING) {
-          bool w0, w1 = false;
-          if (!lambda_mode) {
-            const float tq = (myqs ? thr[1] : thr[0]);
-            w0 = rvalid && rm0 * p.sigma >= tq;
-            w1 = rvalid && rm1 * p.sigma >= tq;
-          } else {
-            w0 = rvalid && (myqs ? cls[1][0] : cls[0][0]) == 1 && ((rm0 - m_true) * p.sigma >= p.log_lambda);
-          }
-          // Every read of S is complete here (tcgen05.wait::ld above); the
-          // fence orders it before the barrier, so that the MMA warp may
-          // overwrite S as soon as it reads a skip decision.
           tc_fence_before();
-          if (simple) {
-            const bool wf = __any_sync(0xffffffffu, !okl);
-            const bool wv = __any_sync(0xffffffffu, w0);
-            const uint32_t n = bar_red_popc(bar_id, 128, lane == 0 ? wf : (lane <= 8 && wv));
-            ok = (n & 7u) == 0u;
-            if (!ok) break;
-            tile_vote = n >= 8u;
-          } else {
-            const uint32_t bits = (__any_sync(0xffffffffu, w0) ? 1u : 0u) |
-                                  ((KS == 2 && __any_sync(0xffffffffu, w1)) ? 2u : 0u);
-            c->vote[s][tb][wq] = bits;  // every lane: same value
+          mbar_arrive(&c->red_full[s][tb]);
+          // Calibration: the slot's first warp records sigma * s_max of each
+          // candidate block once every warp's maxima are in.
+          if (wq == 0) {
+            if (!(ok = wait_all(&c->red_full[s][tb], ph, abort, p.err, ERR_WAIT_RED))) break;
+            if (lane == 0) {
+              for (int q = 0; q < QS; ++q)
+                for (int k = 0; k < KS; ++k) {
+                  if (cls[q][k] != 1) continue;
+                  float mx = -CUDART_INF_F;
+                  for (int w = 0; w < 4; ++w)
+                    if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][tb][w][k]);
+                  const long long idx =
+                      ((long long)h * p.cal_nq + iq_base + q) * p.cal_nk + (J * TILE) / p.Bk + k;
+                  p.blockmax[idx] = mx * p.sigma;
+                }
+            }
+            __syncwarp();
           }
-        }
-        if (!(GATING && !CALIB && simple)) {
-          ok = bar_red_and(bar_id, 128, okl);
-          if (!ok) break;
-        }
-
-        if constexpr (CALIB) {
-          // Calibration: record sigma * s_max for candidate blocks.
-          if (row == 0) {
-            for (int q = 0; q < QS; ++q)
-              for (int k = 0; k < KS; ++k) {
-                if (cls[q][k] != 1) continue;
-                float mx = -CUDART_INF_F;
-                for (int w = 0; w < 4; ++w)
-                  if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][tb][w][k]);
-                const long long idx =
-                    ((long long)h * p.cal_nq + iq_base + q) * p.cal_nk + (J * TILE) / p.Bk + k;
-                p.blockmax[idx] = mx * p.sigma;
-              }
-          }
-          tc_fence_before();
-          mbar_arrive(&c->p_full[s]);
+          mbar_arrive(&c->p_full[s][tb]);
           continue;
         } else {
           // ---- gate: decide every sub-block of this tile
@@ -726,20 +736,46 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 #pragma unroll
             for (int k = 0; k < 2; ++k) keep[q][k] = cls[q][k] != 0;
           if constexpr (GATING) {
-            // OR the warp votes of each query half (warps 0-1 hold rows 0-63).
-            uint32_t vq0, vq1;
-            if (simple) {
-              vq0 = vq1 = tile_vote ? 1u : 0u;
+            bool w0, w1 = false;
+            if (!lambda_mode) {
+              const float tq = (myqs ? thr[1] : thr[0]);
+              w0 = rvalid && rm0 * p.sigma >= tq;
+              w1 = rvalid && rm1 * p.sigma >= tq;
             } else {
-              const uint4 vv = *reinterpret_cast<const uint4*>(&c->vote[s][tb][0]);
-              vq0 = vv.x | vv.y;
-              vq1 = vv.z | vv.w;
-              if (QS == 1) vq0 = vq1 = vq0 | vq1;
+              w0 = rvalid && (myqs ? cls[1][0] : cls[0][0]) == 1 &&
+                   ((rm0 - m_true) * p.sigma >= p.log_lambda);
             }
+            // Every read of S is complete here (tcgen05.wait::ld above); the
+            // fence orders it before the barrier, so that the MMA warp may
+            // overwrite S as soon as it reads a skip decision.
+            tc_fence_before();
+            if (simple) {
+              // One 128x128 semantic block per tile: the hardware barrier
+              // itself carries the vote (no shared-memory traffic, which
+              // queues behind the MMAs' operand reads).  Lane 0 of each warp
+              // counts 1 when some lane of the warp has stopped, lanes 1..8
+              // count 1 each when some row of the warp wants the block, so the
+              // count is F + 8 V with F, V <= 4.
+              const bool wf = __any_sync(0xffffffffu, !okl);
+              const bool wv = __any_sync(0xffffffffu, w0);
+              const uint32_t n = bar_red_popc(bar_id, 128, lane == 0 ? wf : (lane <= 8 && wv));
+              ok = (n & 7u) == 0u;
+              if (!ok) break;
+              if (!diag_tile) keep[0][0] = n >= 8u;
+            } else {
+              c->vote[s][tb][wq] = (__any_sync(0xffffffffu, w0) ? 1u : 0u) |
+                                   ((KS == 2 && __any_sync(0xffffffffu, w1)) ? 2u : 0u);
+              ok = bar_red_and(bar_id, 128, okl);
+              if (!ok) break;
+              // OR the warp votes of each query half (warps 0-1 hold rows 0-63).
+              const uint4 vv = *reinterpret_cast<const uint4*>(&c->vote[s][tb][0]);
+              uint32_t vq0 = vv.x | vv.y, vq1 = vv.z | vv.w;
+              if (QS == 1) vq0 = vq1 = vq0 | vq1;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              if (cls[0][k] == 1) keep[0][k] = (vq0 >> k) & 1u;
-              if (cls[1][k] == 1) keep[1][k] = (vq1 >> k) & 1u;
+              for (int k = 0; k < 2; ++k) {
+                if (cls[0][k] == 1) keep[0][k] = (vq0 >> k) & 1u;
+                if (cls[1][k] == 1) keep[1][k] = (vq1 >> k) & 1u;
+              }
             }
             if (lambda_mode) {
               // Sub-blocks in ascending key order; a row's running max moves
@@ -748,10 +784,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
               if ((myqs ? keep[1][0] : keep[0][0])) m_true = fmaxf(m_true, rm0);
               if (KS == 2) {
                 if (cls[0][1] == 1 || cls[1][1] == 1) {
-                  const bool w1 =
-                      rvalid && (myqs ? cls[1][1] : cls[0][1]) == 1 && ((rm1 - m_true) * p.sigma >= p.log_lambda);
-                  const uint32_t b1 = __any_sync(0xffffffffu, w1) ? 1u : 0u;
-                  c->vote2[s][tb][wq] = b1;
+                  const bool v1 = rvalid && (myqs ? cls[1][1] : cls[0][1]) == 1 &&
+                                  ((rm1 - m_true) * p.sigma >= p.log_lambda);
+                  c->vote2[s][tb][wq] = __any_sync(0xffffffffu, v1) ? 1u : 0u;
+                  // Every thread passed the vote barrier above, so all of them
+                  // reach this one.
                   named_bar_sync(bar_id, 128);
                   const uint4 v2 = *reinterpret_cast<const uint4*>(&c->vote2[s][tb][0]);
                   uint32_t u0 = v2.x | v2.y, u1 = v2.z | v2.w;
@@ -770,7 +807,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             for (int k = 0; k < 2; ++k)
               if (keep[q][k]) decbits |= 1u << (q * 2 + k);
           if (GATING && wq == 0) {  // all 32 lanes: same value, 32 arrivals
-            c->dec[s][tb] = decbits;
+            // Release: a reader that sees this tile's stamp also sees every
+            // S read the decision depended on (the votes it waited for).
+            st_release_u32(&c->dec[s][tb], ((tc & DEC_STAMP_MASK) << DEC_BITS) | decbits);
             mbar_arrive(&c->dec_full[s][tb]);
           }
 
@@ -853,7 +892,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             o_init = true;
           }
           tc_fence_before();
-          mbar_arrive(&c->p_full[s]);
+          mbar_arrive(&c->p_full[s][tb]);
 
           // ---- bookkeeping: bitmap words and block counts (after the
           // hand-off of P, off the path to the next MMA)
@@ -888,8 +927,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         if (bm_on)
           for (int w = bm_idx + lane; w < p.words; w += 32)
             p.bitmap[bm_row + w] = (w == bm_idx) ? bm_word : 0u;
-        const bool okl = wait_bar(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL);
-        if (!(ok = bar_red_and(bar_id, 128, okl))) break;
+        if constexpr (GATING) {
+          const bool okl = wait_bar(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL);
+          if (!(ok = bar_red_and(bar_id, 128, okl))) break;
+        } else {
+          if (!(ok = wait_all(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL))) break;
+        }
         tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         uint16_t* orow = p.o + (long long)si.w * p.o_sb + (long long)h * p.o_sh +

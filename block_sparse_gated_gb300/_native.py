@@ -31,6 +31,8 @@ class FwdParams(ctypes.Structure):
         ("kept_bitmap", c_void_p), ("lse", c_void_p), ("block_counts", c_void_p),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
         ("dtype", c_int), ("flags", ctypes.c_uint),
+        ("block_table", c_void_p), ("block_table_stride", c_int),
+        ("page_size", c_int), ("num_pages", c_int),
     ]
 
 

@@ -72,15 +72,40 @@ def _strides_bhtd(t: torch.Tensor, layout: str, varlen: bool):
     raise ValueError(layout)
 
 
+def _pool_strides(t: torch.Tensor, kv_layout: str):
+    """Element strides {page, head, token}, heads and page size of a K or V
+    page pool: [pages, page_size, Hkv, d] ("pthd") or [pages, Hkv, page_size, d]
+    ("phtd"), d contiguous."""
+    _dtype_code(t)
+    if t.dim() != 4 or t.stride(-1) != 1:
+        raise ValueError("page pools are 4-D with the head dimension contiguous")
+    s = t.stride()
+    if kv_layout == "pthd":
+        return (s[0], s[2], s[1]), t.shape[2], t.shape[1]
+    if kv_layout == "phtd":
+        return (s[0], s[1], s[2]), t.shape[1], t.shape[2]
+    raise ValueError(kv_layout)
+
+
 def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, softmax_scale,
-            mode, thresholds, log_lambda, v_always=False):
+            mode, thresholds, log_lambda, v_always=False, block_table=None, kv_layout="pthd"):
     varlen = cu_seqlens is not None
     if layout is None:
         layout = "htd" if varlen else "bhld"
     qs, Hq, Lq = _strides_bhtd(q, layout, varlen)
-    ks, Hkv, Lk = _strides_bhtd(k, layout, varlen)
-    vs, Hv, Lv = _strides_bhtd(v, layout, varlen)
     os_, Ho, Lo = _strides_bhtd(o, layout, varlen)
+    paged = block_table is not None
+    if paged:
+        ks, Hkv, page = _pool_strides(k, kv_layout)
+        vs, Hv, page_v = _pool_strides(v, kv_layout)
+        if page_v != page or v.shape[0] != k.shape[0]:
+            raise ValueError("K and V pools disagree")
+        if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.stride(1) != 1:
+            raise ValueError("block_table must be an int32 [batch, pages_per_sequence] tensor")
+        Lk = Lv = Lq
+    else:
+        ks, Hkv, Lk = _strides_bhtd(k, layout, varlen)
+        vs, Hv, Lv = _strides_bhtd(v, layout, varlen)
     if not (Lq == Lk == Lv == Lo) or Hv != Hkv or Ho != Hq:
         raise ValueError("Q/K/V/O shapes disagree")
     if not (q.dtype == k.dtype == v.dtype == o.dtype):
@@ -110,6 +135,11 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
     p.log_lambda = float(log_lambda) if log_lambda is not None else 0.0
     p.dtype = _dtype_code(q)
     p.flags = _native.FLAG_V_ALWAYS if v_always else 0
+    if paged:
+        p.block_table = block_table.data_ptr()
+        p.block_table_stride = block_table.stride(0)
+        p.page_size = page
+        p.num_pages = k.shape[0]
     return p
 
 
@@ -125,19 +155,26 @@ def bitmap_shape(num_heads_q: int, *, block_q: int, block_k: int, seqlens) -> tu
 def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="threshold",
             thresholds=None, log_lambda=None, cu_seqlens=None, max_seqlen=None, layout=None,
             out=None, return_bitmap=False, return_lse=False, return_counts=False,
-            workspace=None, stream=None, v_always=False):
+            workspace=None, stream=None, v_always=False, block_table=None, kv_layout="pthd"):
     """Gated causal prefill.  Batched: q [B, Hq, L, d] (layout "bhld") or
     [B, L, Hq, d] ("blhd"); varlen (cu_seqlens int32 on the device): q [Hq, T, d]
     ("htd") or [T, Hq, d] ("thd").  Returns a dict with "out" and, on request,
     "bitmap" (int32 [rows, Hq, words], bit j of word j//32 = keep), "lse"
     (float32 [Hq, rows_of_tokens]) and "counts" (int64 [3]: kept candidates,
     candidates, diagonal-region blocks).  ``v_always`` loads V for skipped
-    tiles too (results unchanged; for measuring what the skipped load saves)."""
+    tiles too (results unchanged; for measuring what the skipped load saves).
+
+    Paged K/V: with ``block_table`` (int32 [batch, pages_per_sequence] on the
+    device), k and v are page pools [pages, page_size, Hkv, d] (``kv_layout``
+    "pthd") or [pages, Hkv, page_size, d] ("phtd"), page_size a multiple of
+    128; key position pos of sequence b is token pos % page_size of page
+    block_table[b, pos // page_size].  q and out keep their layout."""
     if out is None:
         out = torch.empty_like(q)
     p = _params(q, k, v, out, layout=layout, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
                 block_q=block_q, block_k=block_k, softmax_scale=softmax_scale, mode=mode,
-                thresholds=thresholds, log_lambda=log_lambda, v_always=v_always)
+                thresholds=thresholds, log_lambda=log_lambda, v_always=v_always,
+                block_table=block_table, kv_layout=kv_layout)
     L = _native.lib()
     res = {"out": out}
     dev = q.device

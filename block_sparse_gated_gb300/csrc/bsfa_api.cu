@@ -200,38 +200,35 @@ static unsigned* error_word() {
   return static_cast<unsigned*>(ptr);
 }
 
+template <bool CALIB, bool F16, bool G, bool VA, bool PG>
+static cudaError_t dispatch_dn(int d, int nq, const Maps& m, const DevParams& p, int grid,
+                               cudaStream_t st) {
+  if (d == 128) return nq == 2 ? launch_fwd<128, 2, G, CALIB, F16, VA, PG>(m, p, grid, st)
+                               : launch_fwd<128, 1, G, CALIB, F16, VA, PG>(m, p, grid, st);
+  return nq == 2 ? launch_fwd<64, 2, G, CALIB, F16, VA, PG>(m, p, grid, st)
+                 : launch_fwd<64, 1, G, CALIB, F16, VA, PG>(m, p, grid, st);
+}
+
 template <bool CALIB, bool F16>
-static cudaError_t dispatch_t(int d, int nq, bool gating, bool vall, const Maps& m,
+static cudaError_t dispatch_t(int d, int nq, bool gating, bool vall, bool paged, const Maps& m,
                               const DevParams& p, int grid, cudaStream_t st) {
-  if (CALIB) {
-    if (d == 128) return nq == 2 ? launch_fwd<128, 2, true, true, F16, false>(m, p, grid, st)
-                                 : launch_fwd<128, 1, true, true, F16, false>(m, p, grid, st);
-    return nq == 2 ? launch_fwd<64, 2, true, true, F16, false>(m, p, grid, st)
-                   : launch_fwd<64, 1, true, true, F16, false>(m, p, grid, st);
+  if constexpr (CALIB) {
+    return dispatch_dn<true, F16, true, false, false>(d, nq, m, p, grid, st);
+  } else {
+    if (paged)
+      return gating ? dispatch_dn<false, F16, true, false, true>(d, nq, m, p, grid, st)
+                    : dispatch_dn<false, F16, false, false, true>(d, nq, m, p, grid, st);
+    if (gating && vall) return dispatch_dn<false, F16, true, true, false>(d, nq, m, p, grid, st);
+    return gating ? dispatch_dn<false, F16, true, false, false>(d, nq, m, p, grid, st)
+                  : dispatch_dn<false, F16, false, false, false>(d, nq, m, p, grid, st);
   }
-  if (gating && vall) {
-    if (d == 128) return nq == 2 ? launch_fwd<128, 2, true, false, F16, true>(m, p, grid, st)
-                                 : launch_fwd<128, 1, true, false, F16, true>(m, p, grid, st);
-    return nq == 2 ? launch_fwd<64, 2, true, false, F16, true>(m, p, grid, st)
-                   : launch_fwd<64, 1, true, false, F16, true>(m, p, grid, st);
-  }
-  if (d == 128) {
-    if (gating) return nq == 2 ? launch_fwd<128, 2, true, false, F16, false>(m, p, grid, st)
-                               : launch_fwd<128, 1, true, false, F16, false>(m, p, grid, st);
-    return nq == 2 ? launch_fwd<128, 2, false, false, F16, false>(m, p, grid, st)
-                   : launch_fwd<128, 1, false, false, F16, false>(m, p, grid, st);
-  }
-  if (gating) return nq == 2 ? launch_fwd<64, 2, true, false, F16, false>(m, p, grid, st)
-                             : launch_fwd<64, 1, true, false, F16, false>(m, p, grid, st);
-  return nq == 2 ? launch_fwd<64, 2, false, false, F16, false>(m, p, grid, st)
-                 : launch_fwd<64, 1, false, false, F16, false>(m, p, grid, st);
 }
 
 template <bool CALIB>
-static cudaError_t dispatch(bool f16, int d, int nq, bool gating, bool vall, const Maps& m,
-                            const DevParams& p, int grid, cudaStream_t st) {
-  return f16 ? dispatch_t<CALIB, true>(d, nq, gating, vall, m, p, grid, st)
-             : dispatch_t<CALIB, false>(d, nq, gating, vall, m, p, grid, st);
+static cudaError_t dispatch(bool f16, int d, int nq, bool gating, bool vall, bool paged,
+                            const Maps& m, const DevParams& p, int grid, cudaStream_t st) {
+  return f16 ? dispatch_t<CALIB, true>(d, nq, gating, vall, paged, m, p, grid, st)
+             : dispatch_t<CALIB, false>(d, nq, gating, vall, paged, m, p, grid, st);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -290,10 +287,20 @@ static bsfa_status validate(const bsfa_fwd_params* p) {
   if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->o))
     return BSFA_ERR_UNSUPPORTED;
   const int first = p->cu_seqlens ? 1 : 0;
+  const bool paged = p->block_table != nullptr;
   for (int i = first; i < 3; ++i)
     if (!stride_ok(p->q_stride[i]) || !stride_ok(p->k_stride[i]) || !stride_ok(p->v_stride[i]) ||
         !stride_ok(p->o_stride[i]))
       return BSFA_ERR_UNSUPPORTED;
+  if (paged) {
+    // Pages are addressed through the "batch" stride of K and V, in either layout.
+    if (!stride_ok(p->k_stride[0]) || !stride_ok(p->v_stride[0])) return BSFA_ERR_UNSUPPORTED;
+    if (p->page_size <= 0 || p->page_size % TILE != 0) return BSFA_ERR_UNSUPPORTED;
+    if (p->flags & BSFA_FLAG_V_ALWAYS) return BSFA_ERR_UNSUPPORTED;  // no paged V-always kernels
+    if (p->num_pages < 1) return BSFA_ERR_INVALID_ARG;
+    if ((long long)p->block_table_stride * p->page_size < max_len_of(p))
+      return BSFA_ERR_INVALID_ARG;
+  }
   if (p->mode == BSFA_GATE_THRESHOLD && (p->thresholds == nullptr || p->thresholds_nq < 1))
     return BSFA_ERR_INVALID_ARG;
   if (p->mode == BSFA_GATE_LAMBDA && std::isnan(p->log_lambda)) return BSFA_ERR_INVALID_ARG;
@@ -358,13 +365,23 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
     return varlen ? (long long)st[1] * heads : (long long)st[0];
   };
   const bool f16 = p->dtype == BSFA_DTYPE_F16;
+  const bool paged = p->block_table != nullptr;
   if (!make_map(&m.q, p->q, f16, d, p->seqlen, p->num_heads_q, bdim, p->q_stride[2], p->q_stride[1],
-                bstride(p->q_stride, p->num_heads_q)) ||
-      !make_map(&m.k, p->k, f16, d, p->seqlen, p->num_heads_kv, bdim, p->k_stride[2], p->k_stride[1],
-                bstride(p->k_stride, p->num_heads_kv)) ||
-      !make_map(&m.v, p->v, f16, d, p->seqlen, p->num_heads_kv, bdim, p->v_stride[2], p->v_stride[1],
-                bstride(p->v_stride, p->num_heads_kv)))
+                bstride(p->q_stride, p->num_heads_q)))
     return BSFA_ERR_CUDA;
+  if (paged) {
+    // Page pools: {d, tokens of a page, KV heads, pages}.
+    if (!make_map(&m.k, p->k, f16, d, p->page_size, p->num_heads_kv, p->num_pages, p->k_stride[2],
+                  p->k_stride[1], p->k_stride[0]) ||
+        !make_map(&m.v, p->v, f16, d, p->page_size, p->num_heads_kv, p->num_pages, p->v_stride[2],
+                  p->v_stride[1], p->v_stride[0]))
+      return BSFA_ERR_CUDA;
+  } else if (!make_map(&m.k, p->k, f16, d, p->seqlen, p->num_heads_kv, bdim, p->k_stride[2],
+                       p->k_stride[1], bstride(p->k_stride, p->num_heads_kv)) ||
+             !make_map(&m.v, p->v, f16, d, p->seqlen, p->num_heads_kv, bdim, p->v_stride[2],
+                       p->v_stride[1], bstride(p->v_stride, p->num_heads_kv))) {
+    return BSFA_ERR_CUDA;
+  }
 
   DevParams dp{};
   dp.o = static_cast<uint16_t*>(p->o);
@@ -395,6 +412,9 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   dp.seqinfo = cv.seqinfo;
   dp.tiles = cv.tiles;
   dp.ntiles_total = cv.ntot;
+  dp.btab = paged ? p->block_table : nullptr;
+  dp.bt_stride = paged ? p->block_table_stride : 0;
+  dp.tiles_per_page = paged ? p->page_size / TILE : 1;
   dp.err = error_word();
   if (dp.err == nullptr) return BSFA_ERR_CUDA;
 
@@ -413,7 +433,8 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   if (sms <= 0) return BSFA_ERR_CUDA;
   const int grid = (int)(units < sms ? units : sms);
   const bool vall = (p->flags & BSFA_FLAG_V_ALWAYS) != 0;
-  if (dispatch<false>(f16, d, nq, p->mode != BSFA_GATE_NONE, vall, m, dp, grid, stream) != cudaSuccess)
+  if (dispatch<false>(f16, d, nq, p->mode != BSFA_GATE_NONE, vall, paged, m, dp, grid, stream) !=
+      cudaSuccess)
     return BSFA_ERR_CUDA;
   return BSFA_OK;
 }
@@ -512,7 +533,8 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
                   (long long)k_stride[0] * Hkv))
       return BSFA_ERR_CUDA;
     m.v = m.k;
-    if (dispatch<true>(f16, d, nq, true, false, m, dp, grid, stream) != cudaSuccess) return BSFA_ERR_CUDA;
+    if (dispatch<true>(f16, d, nq, true, false, false, m, dp, grid, stream) != cudaSuccess)
+      return BSFA_ERR_CUDA;
     sa.sample = n;
     select_kernel<<<dim3(nqb, Hq), sel_threads, sel_smem, stream>>>(sa);
     if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;

@@ -77,8 +77,23 @@ struct DevParams {
   const int* ntiles_total;
   float* blockmax;            // calibration: [Hq][cal_nq][cal_nk]
   int cal_nq, cal_nk;
+  // Paged K/V: null for contiguous K/V.  Key tile J of sequence b lives in
+  // page btab[b * bt_stride + J / tiles_per_page], 128-token slot
+  // J % tiles_per_page (a 128-key tile never straddles two pages).
+  const int* btab;
+  int bt_stride, tiles_per_page;
   unsigned* err;
 };
+
+// TMA coordinates (token, outermost) of key tile J of sequence b: contiguous
+// K/V address it by the sequence's first token and batch index; paged K/V by
+// the token slot inside its page and the page index from the block table.
+template <bool PAGED>
+__device__ __forceinline__ int2 kv_tile_coord(const DevParams& p, const int4& si, int b, int J) {
+  if constexpr (!PAGED) return make_int2(si.x + J * TILE, si.w);
+  const int pg = __ldg(p.btab + (long long)b * p.bt_stride + J / p.tiles_per_page);
+  return make_int2((J % p.tiles_per_page) * TILE, pg);
+}
 
 template <int D, int NQ>
 struct Ctrl {
@@ -211,6 +226,24 @@ __device__ __forceinline__ int block_class(int i, int j, int Bq, int Bk, int L) 
   return 0;
 }
 
+// Zero rows [first_row, 128) of a 128-row tile in shared memory as TMA wrote
+// it (D/64 swizzled halves of 128 rows x 128 bytes; the 128-byte swizzle only
+// permutes 16-byte chunks inside a row, so whole rows are zeroed in place).
+// All 32 lanes of the calling warp take part; the proxy fence and the warp
+// barrier order the writes before an MMA that the warp then issues.
+template <int D>
+__device__ __forceinline__ void zero_tile_rows(uint8_t* tile, int first_row, int lane) {
+  constexpr int NHALF = D / 64;
+  const int chunks = (TILE - first_row) * NHALF * 8;
+  for (int c = lane; c < chunks; c += 32) {
+    const int r = first_row + c / (NHALF * 8);
+    const int hf = (c / 8) % NHALF, ch = c % 8;
+    *reinterpret_cast<uint4*>(tile + hf * (TILE * 128) + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_shared();
+  __syncwarp();
+}
+
 // S = Q K^T for one slot: D/16 K-steps of M=128, N=128, K=16.  Operand
 // halves (64 columns, 16 KB each) sit TILE*128 bytes apart.
 template <int D, int NQ>
@@ -233,7 +266,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 }
 
 // VALL (gated only): load V for every visible tile, kept or not.
-template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL>
+// PAGED: K and V come from page pools through the block table.
+template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
 __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     bsfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -340,10 +374,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                               ERR_WAIT_K_EMPTY)))
             break;
           if (elect_one()) {
+            const int2 kc2 = kv_tile_coord<PAGED>(p, si, t.x, J + 1);
             mbar_arrive_expect_tx(&c->k_full[st], TB);
             for (int hf = 0; hf < NHALF; ++hf)
-              tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64,
-                          si.x + (J + 1) * TILE, kvh, si.w);
+              tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64, kc2.x, kvh,
+                          kc2.y);
           }
           __syncwarp();
           ++kc;
@@ -356,10 +391,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                                 ERR_WAIT_V_EMPTY)))
               break;
             if (elect_one()) {
+              const int2 vc2 = kv_tile_coord<PAGED>(p, si, t.x, J);
               mbar_arrive_expect_tx(&c->v_full[st], TB);
               for (int hf = 0; hf < NHALF; ++hf)
-                tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64,
-                            si.x + J * TILE, kvh, si.w);
+                tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64, vc2.x, kvh,
+                            vc2.y);
             }
             __syncwarp();
             ++vc;
@@ -413,10 +449,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                               ERR_WAIT_V_EMPTY)))
             break;
           if (elect_one()) {
+            const int2 vc2 = kv_tile_coord<PAGED>(p, si, t.x, J);
             mbar_arrive_expect_tx(&c->v_full[st], TB);
             for (int hf = 0; hf < NHALF; ++hf)
-              tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64,
-                          si.x + J * TILE, kvh, si.w);
+              tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64, vc2.x, kvh,
+                          vc2.y);
           }
           __syncwarp();
           ++vc;
@@ -508,6 +545,13 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                                              ERR_WAIT_V_FULL)))
                   break;
                 vready = true;
+                if (PAGED && J == nkt - 1) {
+                  // Keys of the last tile past the sequence end: a paged pool
+                  // may hold anything there (NaN included), and P = 0 does
+                  // not cancel NaN in P.V.
+                  const int valid = p.seqinfo[t.x].y - J * TILE;
+                  if (valid < TILE) zero_tile_rows<D>(sV + vst * TB, valid, lane);
+                }
               }
               if (first_mask & (1u << s)) {
                 if (!(ok = wait_all(&c->o_empty[s], (uc & 1) ^ 1, abort, p.err,

@@ -12,8 +12,8 @@ struct Maps {
   CUtensorMap q, k, v;
 };
 
-// Launches bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL> with its shared-memory size.
-template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL>
+// Launches bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL, PAGED> with its shared-memory size.
+template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
 cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream);
 
 }  // namespace bsfa

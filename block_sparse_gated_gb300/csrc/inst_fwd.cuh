@@ -4,10 +4,10 @@
 
 namespace bsfa {
 
-template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL>
+template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
 cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream) {
   using LY = Layout<D, NQ, CALIB>;
-  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL>;
+  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL, PAGED>;
   static bool configured[64] = {};  // the attribute is per device; set once on each
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -33,6 +33,8 @@ cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t
 
 }  // namespace bsfa
 
-#define BSFA_INSTANTIATE(D, NQ, G, C, F) BSFA_INSTANTIATE_V(D, NQ, G, C, F, false)
-#define BSFA_INSTANTIATE_V(D, NQ, G, C, F, VA) \
-  template cudaError_t bsfa::launch_fwd<D, NQ, G, C, F, VA>(const Maps&, const DevParams&, int, cudaStream_t);
+#define BSFA_INSTANTIATE(D, NQ, G, C, F) BSFA_INSTANTIATE_VP(D, NQ, G, C, F, false, false)
+#define BSFA_INSTANTIATE_V(D, NQ, G, C, F, VA) BSFA_INSTANTIATE_VP(D, NQ, G, C, F, VA, false)
+#define BSFA_INSTANTIATE_VP(D, NQ, G, C, F, VA, PG)                                          \
+  template cudaError_t bsfa::launch_fwd<D, NQ, G, C, F, VA, PG>(const Maps&, const DevParams&, \
+                                                               int, cudaStream_t);

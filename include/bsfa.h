@@ -139,6 +139,26 @@ typedef struct {
                                  any other value is BSFA_ERR_UNSUPPORTED */
   unsigned int flags;         /* bsfa_flag bits (0 = default); unknown bits are
                                  BSFA_ERR_UNSUPPORTED */
+  /* Paged K/V, the layout a serving KV cache uses ("FlashPrefill V2" summary,
+   * agihunt.info: the sparse kernel reads K/V through the page table, so it
+   * plugs into a paged cache with continuous batching).  block_table == NULL
+   * (a zeroed struct) keeps the contiguous K/V layouts above.  When set:
+   *   - k and v point to page pools: page p holds page_size consecutive tokens
+   *     of every KV head; element (p, h, t, :) sits at
+   *     base + p*stride[0] + h*stride[1] + t*stride[2] (the "batch" stride
+   *     addresses pages), e.g. [num_pages, page_size, Hkv, d];
+   *   - key position pos of sequence b is token pos % page_size of page
+   *     block_table[b*block_table_stride + pos/page_size];
+   *   - q, o, lse and the bitmap keep their batched or varlen layout.
+   * Pool rows past a sequence's last key may hold anything, NaN included:
+   * the kernel zeroes them in shared memory before they reach P.V.  A table
+   * entry outside [0, num_pages) reads as zero keys and values (the TMA
+   * bounds check) and never addresses memory outside the pools. */
+  const int32_t* block_table; /* device int32 [batch][block_table_stride] */
+  int block_table_stride;     /* entries per sequence, >= ceil(max_len / page_size) */
+  int page_size;              /* tokens per page: a positive multiple of 128, else
+                                 BSFA_ERR_UNSUPPORTED */
+  int num_pages;              /* pages in each pool (>= 1) */
 } bsfa_fwd_params;
 
 /* Bytes of workspace bsfa_prefill_fwd needs for these parameters (reads the

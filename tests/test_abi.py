@@ -91,18 +91,47 @@ def test_params_struct_layout_matches_header(libpath):
     from block_sparse_gated_gb300 import _native
     src = (
         '#include <stddef.h>\n#include <stdio.h>\n#include "bsfa.h"\n'
-        'int main(void) { printf("%zu %zu %zu\\n", sizeof(bsfa_fwd_params), '
-        'offsetof(bsfa_fwd_params, dtype), offsetof(bsfa_fwd_params, flags)); '
+        'int main(void) { printf("%zu %zu %zu %zu %zu\\n", sizeof(bsfa_fwd_params), '
+        'offsetof(bsfa_fwd_params, dtype), offsetof(bsfa_fwd_params, flags), '
+        'offsetof(bsfa_fwd_params, block_table), offsetof(bsfa_fwd_params, num_pages)); '
         'return 0; }\n')
     with tempfile.TemporaryDirectory() as tmp:
         c = os.path.join(tmp, "probe.c")
         exe = os.path.join(tmp, "probe")
         open(c, "w").write(src)
         subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
-        size, off_dt, off_fl = map(int, subprocess.run([exe], capture_output=True, text=True,
-                                                         check=True).stdout.split())
+        got = tuple(map(int, subprocess.run([exe], capture_output=True, text=True,
+                                            check=True).stdout.split()))
     F = _native.FwdParams
-    assert (ctypes.sizeof(F), F.dtype.offset, F.flags.offset) == (size, off_dt, off_fl)
+    assert (ctypes.sizeof(F), F.dtype.offset, F.flags.offset, F.block_table.offset,
+            F.num_pages.offset) == got
+
+
+def test_paged_parameters_are_validated_on_the_host(libpath):
+    """Paged K/V: page size, pool size and table width are checked before any
+    launch (the tensor pointers here are never dereferenced)."""
+    import ctypes
+    from block_sparse_gated_gb300 import _native
+    L = _native.lib()
+    p = _native.FwdParams()
+    p.batch, p.num_heads_q, p.num_heads_kv, p.seqlen, p.head_dim = 2, 4, 2, 1000, 128
+    p.block_q = p.block_k = 128
+    p.mode = 2
+    p.q = p.k = p.v = p.o = 1 << 20  # 16-byte aligned stand-ins, never read
+    p.q_stride[:] = p.o_stride[:] = (4 * 1000 * 128, 1000 * 128, 128)
+    p.k_stride[:] = p.v_stride[:] = (256 * 2 * 128, 128, 2 * 128)  # [pages, 256, Hkv, d]
+    p.block_table, p.block_table_stride, p.page_size, p.num_pages = 1 << 12, 4, 200, 16
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # page size not a multiple of 128
+    p.page_size = 256
+    p.num_pages = 0
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # empty pool
+    p.num_pages, p.block_table_stride = 16, 3
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # 3 pages of 256 < 1000 tokens
+    p.block_table_stride = 4
+    p.k_stride[0] = 100  # page stride not a multiple of 8 elements
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2
+    p.k_stride[0] = 256 * 2 * 128
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 5  # all fine up to the missing workspace
 
 
 def test_mixed_element_types_are_rejected_before_the_library():

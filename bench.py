@@ -270,6 +270,7 @@ def run_ours(args, rank, world, local_rank):
     }
 
     if not args.no_sweep and rank == 0:
+        result["paged_kv"] = paged_leg(q, k, v, slices, ks, outs, Bq, Bk, dev)
         result["lambda_sweep"] = lambda_sweep(dev, args)
         result["llama8b_L32768"] = llama_32k_leg(dev)
         result["varlen_8seq_32layer"] = varlen_32layer_leg(dev)
@@ -279,6 +280,48 @@ def run_ours(args, rank, world, local_rank):
         result["cpu_baseline"] = cpu_baseline(args.workload, W, cnts)
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def paged_leg(q, k, v, slices, ks, outs, Bq, Bk, dev, page=256, reps=3):
+    """The k=128 slice of the same layer with K and V read from page pools
+    ([pages, 256, Hkv, d], pages in a seeded random order) through a block
+    table, against the contiguous call; the outputs must be identical."""
+    import torch
+
+    import block_sparse_gated_gb300 as bsfa
+    i = ks.index(128) if 128 in ks else 0
+    L = k.shape[2]
+    n_pages = (L + page - 1) // page
+    perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(5)).to(dev)
+
+    def pool(t):
+        pad = n_pages * page - L
+        x = torch.nn.functional.pad(t[0].transpose(0, 1), (0, 0, 0, 0, 0, pad))
+        x = x.reshape(n_pages, page, t.shape[1], t.shape[3])
+        out = torch.empty_like(x)
+        out[perm] = x
+        return out
+
+    kp, vp = pool(k), pool(v)
+    table = perm.to(torch.int32)[None].contiguous()
+    ref = outs[i]
+    got = torch.empty_like(ref)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    bsfa.prefill(q, k, v, block_q=Bq, block_k=Bk, mode="threshold", thresholds=slices[i],
+                 out=ref, workspace=ws)
+    bsfa.prefill(q, kp, vp, block_q=Bq, block_k=Bk, mode="threshold", thresholds=slices[i],
+                 out=got, workspace=ws, block_table=table)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(got, ref))
+    ms_c = _timed(lambda: bsfa.prefill(q, k, v, block_q=Bq, block_k=Bk, mode="threshold",
+                                       thresholds=slices[i], out=ref, workspace=ws), reps)
+    ms_p = _timed(lambda: bsfa.prefill(q, kp, vp, block_q=Bq, block_k=Bk, mode="threshold",
+                                       thresholds=slices[i], out=got, workspace=ws,
+                                       block_table=table), reps)
+    del kp, vp
+    return {"k": ks[i], "page_size": page, "pages": n_pages, "order": "seeded random permutation",
+            "ms_contiguous": round(ms_c, 3), "ms_paged": round(ms_p, 3),
+            "paged_over_contiguous": round(ms_p / ms_c, 4), "outputs_identical": same}
 
 
 def e2e(q, k, v, slices, flops, Bq, Bk, args, dev):

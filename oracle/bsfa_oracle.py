@@ -27,6 +27,11 @@ Sources (page title, section):
     nothing to the numerator or the denominator; the output is attention
     renormalised over the retained blocks.
   - "A Worked Example": maxima 1, 4, 2, 5, 3.5 against T = 3 keep 4, 5, 3.5.
+* "FlashPrefill V2: Block-Sparse Prefill Attention for Long-Context LLM
+  Serving" (agihunt.info summary), mean correction (optional here): every
+  pruned block J enters as a zero-order stand-in built from its mean key and
+  mean value, |B_J| e^{sbar_J} vbar_J in the numerator and |B_J| e^{sbar_J} in
+  the denominator.
 * "Skipping attention blocks was the easy part" (yash-agarwal.org, BLASST in
   an SM100 prefill kernel), section "Vote, then skip": skip a block when its
   local max minus the running max is below ln(lambda) for every row
@@ -48,6 +53,11 @@ the design doc with its reason):
   region last; the running max m_r starts at -inf, so the first visited
   candidate is always kept.  ln(lambda) is a natural log.
 * Rows and keys past the sequence end take no part in anything.
+* Mean correction: sbar_J = sigma * q_r . kbar_J for each row r; |B_J| is the
+  number of keys of block J (Bk for every candidate); only skipped candidate
+  blocks get a stand-in (the diagonal region is always kept); the gate's
+  decisions are taken without the stand-ins (the lambda running max sees
+  real scores only).
 
 Every function below works on one sequence at a time with layout
 q: [Hq, L, d], k/v: [Hkv, L, d], all float64 (bf16 inputs widen exactly).
@@ -210,33 +220,61 @@ def decision_statistics(q_h, k_h, i, Bq, Bk, sigma, order=None,
 # Aggregation": a skipped block is absent from numerator and denominator).
 # ---------------------------------------------------------------------------
 def attend_kept(s: np.ndarray, v_h: np.ndarray, keep: dict[int, bool],
-                Bk: int) -> tuple[np.ndarray, np.ndarray]:
+                Bk: int, stand_in=None) -> tuple[np.ndarray, np.ndarray]:
     """out[r] = sum_{c in K_r} e^{s[r,c] - M_r} v[c] / Z_r and
-    lse[r] = M_r + ln Z_r, K_r = visible keys of kept blocks."""
+    lse[r] = M_r + ln Z_r, K_r = visible keys of kept blocks.
+
+    stand_in: optional (logits [rows, n], values [n, d]) of extra terms that
+    join the numerator and the denominator (mean correction); a logit that
+    already carries ln|B_J| weighs the term |B_J| times."""
     ncols = s.shape[1]
     col_kept = np.zeros(ncols, dtype=bool)
     for j, kept in keep.items():
         if kept:
             col_kept[j * Bk:min((j + 1) * Bk, ncols)] = True
     sk = np.where(col_kept[None, :], s, NEG_INF)
+    vals = v_h[:ncols]
+    if stand_in is not None and stand_in[0].shape[1] > 0:
+        sk = np.concatenate([sk, stand_in[0]], axis=1)
+        vals = np.concatenate([vals, stand_in[1]], axis=0)
     M = np.max(sk, axis=1, keepdims=True)
     e = np.exp(sk - M)
     Z = np.sum(e, axis=1, keepdims=True)
-    out = (e @ v_h[:ncols]) / Z
+    out = (e @ vals) / Z
     lse = (M + np.log(Z))[:, 0]
     return out, lse
+
+
+def mean_stand_ins(q_rows: np.ndarray, k_h: np.ndarray, v_h: np.ndarray,
+                   keep: dict[int, bool], i: int, Bq: int, Bk: int, L: int,
+                   sigma: float) -> tuple[np.ndarray, np.ndarray]:
+    """Mean correction ("FlashPrefill V2" summary): for every skipped
+    candidate block J of query block i, with |B_J| keys, mean key kbar_J and
+    mean value vbar_J, the row-r logit sigma * q_r . kbar_J + ln|B_J| and the
+    value vbar_J.  Returns (logits [rows, n], values [n, d])."""
+    skipped = [j for j, kept in sorted(keep.items())
+               if not kept and block_class(i, j, Bq, Bk, L) == CANDIDATE]
+    logits = np.zeros((q_rows.shape[0], len(skipped)))
+    vbar = np.zeros((len(skipped), v_h.shape[1]))
+    for n, j in enumerate(skipped):
+        c0, c1 = j * Bk, min((j + 1) * Bk, L)
+        kbar = k_h[c0:c1].mean(axis=0)
+        vbar[n] = v_h[c0:c1].mean(axis=0)
+        logits[:, n] = sigma * (q_rows @ kbar) + math.log(c1 - c0)
+    return logits, vbar
 
 
 # ---------------------------------------------------------------------------
 # One query block, one head: the unit everything else loops over.
 # ---------------------------------------------------------------------------
 def query_block(q_h, k_h, v_h, i, *, Bq, Bk, sigma, mode, T_hi=None,
-                log_lambda=None, order=None, keep_override=None):
+                log_lambda=None, order=None, keep_override=None, mean_correction=False):
     """Gated attention for query block i of one head.
 
     mode: "threshold", "lambda" or "dense" (every visible block kept).
     keep_override: optional {j: bool} that replaces the decisions for the
     listed candidate blocks (used by tests to evaluate a given keep set).
+    mean_correction: add the mean stand-in of every skipped candidate block.
 
     Returns dict(out [rows, d], lse [rows], keep {j: bool}, smax {j: float})."""
     L = q_h.shape[0]
@@ -255,7 +293,10 @@ def query_block(q_h, k_h, v_h, i, *, Bq, Bk, sigma, mode, T_hi=None,
             if block_class(i, j, Bq, Bk, L) == CANDIDATE:
                 keep[j] = bool(kept)
     smax = {j: tile_max(s, j, Bk) for j in keep}
-    out, lse = attend_kept(s, v_h, keep, Bk)
+    stand_in = None
+    if mean_correction:
+        stand_in = mean_stand_ins(q_h[rows], k_h, v_h, keep, i, Bq, Bk, L, sigma)
+    out, lse = attend_kept(s, v_h, keep, Bk, stand_in)
     return {"out": out, "lse": lse, "keep": keep, "smax": smax}
 
 
@@ -266,13 +307,15 @@ def _kv_head(h: int, Hq: int, Hkv: int) -> int:
 
 
 def prefill(q, k, v, *, Bq, Bk, sigma=None, mode="threshold",
-            thresholds=None, log_lambda=None, order_fn=None, blocks=None):
+            thresholds=None, log_lambda=None, order_fn=None, blocks=None,
+            mean_correction=False):
     """Gated causal prefill of one sequence.
 
     q: [Hq, L, d]; k, v: [Hkv, L, d] (float64 or anything np.float64 takes).
     thresholds: [Hq, nT] (threshold mode).  sigma defaults to 1/sqrt(d).
     order_fn(h, i) -> visit order (lambda mode only; default ascending).
     blocks: optional iterable of (h, i) to evaluate; others are left NaN.
+    mean_correction: add the mean stand-ins of skipped candidate blocks.
 
     Returns dict(out [Hq, L, d], lse [Hq, L], keep [Hq, nq, nk] bool,
     visible [Hq, nq, nk] bool, candidate [Hq, nq, nk] bool)."""
@@ -297,7 +340,8 @@ def prefill(q, k, v, *, Bq, Bk, sigma=None, mode="threshold",
             T_hi = float(thresholds[h][threshold_index(i, len(thresholds[h]))])
         order = order_fn(h, i) if (order_fn is not None and mode == "lambda") else None
         res = query_block(q[h], k[kh], v[kh], i, Bq=Bq, Bk=Bk, sigma=sigma,
-                          mode=mode, T_hi=T_hi, log_lambda=log_lambda, order=order)
+                          mode=mode, T_hi=T_hi, log_lambda=log_lambda, order=order,
+                          mean_correction=mean_correction)
         r0, r1 = i * Bq, min((i + 1) * Bq, L)
         out[h, r0:r1] = res["out"]
         lse[h, r0:r1] = res["lse"]

@@ -386,3 +386,76 @@ def test_effective_flops_counts():
     keep = np.array([[[True, False], [True, True]]])
     vis = np.array([[[True, False], [True, True]]])
     assert orc.effective_flops(keep, vis, 2, 2, 3) == 2 * 2 * 2 * 3 * (3 + 3)
+
+
+# ---------------------------------------------------------------------------
+# Mean correction ("FlashPrefill V2" summary: a pruned block J enters the
+# numerator as |B_J| e^{sbar_J} vbar_J and the denominator as |B_J| e^{sbar_J})
+# ---------------------------------------------------------------------------
+def _constant_blocks(Hkv, L, d, B, seed):
+    """K and V whose rows are identical inside every B-row block."""
+    nb = orc.num_blocks(L, B)
+    kb, vb = _rand((Hkv, nb, d), seed), _rand((Hkv, nb, d), seed + 1)
+    return np.repeat(kb, B, axis=1)[:, :L], np.repeat(vb, B, axis=1)[:, :L]
+
+
+@pytest.mark.parametrize("Bq,Bk,L", [(8, 8, 61), (1, 1, 9), (8, 4, 40), (4, 8, 37)])
+def test_mean_correction_is_exact_for_constant_blocks(Bq, Bk, L):
+    """When every key (and value) of a block equals the block mean, the stand-in
+    reproduces the block's exact contribution: the corrected output with every
+    candidate skipped equals dense causal attention."""
+    Hq, Hkv, d = 2, 1, 5
+    q = _rand((Hq, L, d), 70)
+    k, v = _constant_blocks(Hkv, L, d, Bk, 71)
+    dense = _sdpa(q, _repeat_kv(k, Hq), _repeat_kv(v, Hq), causal=True, sigma=0.5)
+    T = np.full((Hq, 1), np.inf)
+    r = orc.prefill(q, k, v, Bq=Bq, Bk=Bk, sigma=0.5, thresholds=T, mean_correction=True)
+    assert r["keep"][r["candidate"]].sum() == 0  # every candidate skipped
+    assert np.abs(r["out"] - dense).max() < 1e-12
+    plain = orc.prefill(q, k, v, Bq=Bq, Bk=Bk, sigma=0.5, thresholds=T)
+    if r["candidate"].any():
+        assert np.abs(plain["out"] - dense).max() > 1e-3  # the stand-ins did the work
+
+
+@pytest.mark.parametrize("Bq,Bk,L", [(8, 8, 70), (8, 4, 50)])
+def test_mean_correction_equals_replicated_mean_keys(Bq, Bk, L):
+    """Independent form: each skipped candidate block replaced by |B_J| copies
+    of its mean key and value, then plain masked attention (library SDPA)."""
+    Hq, Hkv, d, sigma = 1, 1, 6, 0.4
+    q, k, v = _rand((Hq, L, d), 80), _rand((Hkv, L, d), 81), _rand((Hkv, L, d), 82)
+    rng = np.random.default_rng(83)
+    T = rng.uniform(1.8, 2.8, size=(Hq, orc.num_blocks(L, Bq)))
+    r = orc.prefill(q, k, v, Bq=Bq, Bk=Bk, sigma=sigma, thresholds=T, mean_correction=True)
+    for i in range(orc.num_blocks(L, Bq)):
+        r0, r1 = i * Bq, min((i + 1) * Bq, L)
+        keys, vals, vis = [], [], []
+        for j in range(orc.num_blocks(L, Bk)):
+            cls = orc.block_class(i, j, Bq, Bk, L)
+            if cls is None:
+                continue
+            c0, c1 = j * Bk, min((j + 1) * Bk, L)
+            if r["keep"][0, i, j]:
+                for c in range(c0, c1):
+                    keys.append(k[0, c]), vals.append(v[0, c])
+                    vis.append([c <= row for row in range(r0, r1)])
+            else:
+                for _ in range(c1 - c0):
+                    keys.append(k[0, c0:c1].mean(axis=0)), vals.append(v[0, c0:c1].mean(axis=0))
+                    vis.append([True] * (r1 - r0))
+        mask = np.array(vis).T
+        ref = _sdpa(q[:, r0:r1], np.array(keys)[None], np.array(vals)[None], mask=mask,
+                    sigma=sigma)
+        assert np.abs(r["out"][0, r0:r1] - ref[0]).max() < 1e-12, f"query block {i}"
+    assert (~r["keep"][r["candidate"]]).sum() > 0  # some blocks were skipped
+
+
+def test_mean_correction_without_skips_changes_nothing():
+    Hq, Hkv, L, d = 2, 2, 90, 4
+    q, k, v = _rand((Hq, L, d), 90), _rand((Hkv, L, d), 91), _rand((Hkv, L, d), 92)
+    T = np.full((Hq, 1), -np.inf)
+    a = orc.prefill(q, k, v, Bq=16, Bk=16, thresholds=T)
+    b = orc.prefill(q, k, v, Bq=16, Bk=16, thresholds=T, mean_correction=True)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
+    lam = orc.prefill(q, k, v, Bq=16, Bk=16, mode="lambda", log_lambda=-np.inf,
+                      mean_correction=True)
+    assert np.array_equal(lam["out"], a["out"])

@@ -271,6 +271,7 @@ def run_ours(args, rank, world, local_rank):
 
     if not args.no_sweep and rank == 0:
         result["paged_kv"] = paged_leg(q, k, v, slices, ks, outs, Bq, Bk, dev)
+        result["mean_correction"] = mean_correction_leg(q, k, v, slices, ks, Bq, Bk, dev)
         result["lambda_sweep"] = lambda_sweep(dev, args)
         result["llama8b_L32768"] = llama_32k_leg(dev)
         result["varlen_8seq_32layer"] = varlen_32layer_leg(dev)
@@ -322,6 +323,31 @@ def paged_leg(q, k, v, slices, ks, outs, Bq, Bk, dev, page=256, reps=3):
     return {"k": ks[i], "page_size": page, "pages": n_pages, "order": "seeded random permutation",
             "ms_contiguous": round(ms_c, 3), "ms_paged": round(ms_p, 3),
             "paged_over_contiguous": round(ms_p / ms_c, 4), "outputs_identical": same}
+
+
+def mean_correction_leg(q, k, v, slices, ks, Bq, Bk, dev, reps=3):
+    """Cost of the mean-correction option on the k=128 slice: the same gate
+    (identical bitmap), plus the block-mean pass and one correction tile per
+    128 candidate blocks of every query tile."""
+    import torch
+
+    import block_sparse_gated_gb300 as bsfa
+    i = ks.index(128) if 128 in ks else 0
+    out = torch.empty_like(q)
+    kw = dict(block_q=Bq, block_k=Bk, mode="threshold", thresholds=slices[i], out=out)
+    need = bsfa.api.prefill_workspace_bytes(q, k, v, mean_correction=True, **kw)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    a = bsfa.prefill(q, k, v, return_bitmap=True, workspace=ws, **kw)["bitmap"].clone()
+    b = bsfa.prefill(q, k, v, return_bitmap=True, workspace=ws, mean_correction=True,
+                     **kw)["bitmap"]
+    torch.cuda.synchronize()
+    ms_plain = _timed(lambda: bsfa.prefill(q, k, v, workspace=ws, **kw), reps)
+    ms_corr = _timed(lambda: bsfa.prefill(q, k, v, workspace=ws, mean_correction=True, **kw),
+                     reps)
+    return {"k": ks[i], "ms_plain": round(ms_plain, 3), "ms_corrected": round(ms_corr, 3),
+            "corrected_over_plain": round(ms_corr / ms_plain, 4),
+            "bitmap_identical": bool(torch.equal(a, b)),
+            "workspace_bytes": int(need)}
 
 
 def e2e(q, k, v, slices, flops, Bq, Bk, args, dev):

@@ -40,6 +40,7 @@ class FwdParams(ctypes.Structure):
 DTYPE_BF16, DTYPE_F16 = 0, 1
 # bsfa_flag
 FLAG_V_ALWAYS = 1
+FLAG_MEAN_CORRECTION = 2
 
 
 # Every exported symbol and its C signature: (name, restype, argtypes).

@@ -88,7 +88,8 @@ def _pool_strides(t: torch.Tensor, kv_layout: str):
 
 
 def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, softmax_scale,
-            mode, thresholds, log_lambda, v_always=False, block_table=None, kv_layout="pthd"):
+            mode, thresholds, log_lambda, v_always=False, block_table=None, kv_layout="pthd",
+            mean_correction=False):
     varlen = cu_seqlens is not None
     if layout is None:
         layout = "htd" if varlen else "bhld"
@@ -134,7 +135,8 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
         p.thresholds, p.thresholds_nq = None, 0
     p.log_lambda = float(log_lambda) if log_lambda is not None else 0.0
     p.dtype = _dtype_code(q)
-    p.flags = _native.FLAG_V_ALWAYS if v_always else 0
+    p.flags = (_native.FLAG_V_ALWAYS if v_always else 0) | \
+        (_native.FLAG_MEAN_CORRECTION if mean_correction else 0)
     if paged:
         p.block_table = block_table.data_ptr()
         p.block_table_stride = block_table.stride(0)
@@ -155,7 +157,8 @@ def bitmap_shape(num_heads_q: int, *, block_q: int, block_k: int, seqlens) -> tu
 def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="threshold",
             thresholds=None, log_lambda=None, cu_seqlens=None, max_seqlen=None, layout=None,
             out=None, return_bitmap=False, return_lse=False, return_counts=False,
-            workspace=None, stream=None, v_always=False, block_table=None, kv_layout="pthd"):
+            workspace=None, stream=None, v_always=False, block_table=None, kv_layout="pthd",
+            mean_correction=False):
     """Gated causal prefill.  Batched: q [B, Hq, L, d] (layout "bhld") or
     [B, L, Hq, d] ("blhd"); varlen (cu_seqlens int32 on the device): q [Hq, T, d]
     ("htd") or [T, Hq, d] ("thd").  Returns a dict with "out" and, on request,
@@ -168,13 +171,17 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
     device), k and v are page pools [pages, page_size, Hkv, d] (``kv_layout``
     "pthd") or [pages, Hkv, page_size, d] ("phtd"), page_size a multiple of
     128; key position pos of sequence b is token pos % page_size of page
-    block_table[b, pos // page_size].  q and out keep their layout."""
+    block_table[b, pos // page_size].  q and out keep their layout.
+
+    ``mean_correction``: every skipped candidate block enters the softmax
+    through a stand-in built from its mean key and mean value, weighted by its
+    key count (threshold and lambda modes, 128 x 128 blocks, contiguous K/V)."""
     if out is None:
         out = torch.empty_like(q)
     p = _params(q, k, v, out, layout=layout, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
                 block_q=block_q, block_k=block_k, softmax_scale=softmax_scale, mode=mode,
                 thresholds=thresholds, log_lambda=log_lambda, v_always=v_always,
-                block_table=block_table, kv_layout=kv_layout)
+                block_table=block_table, kv_layout=kv_layout, mean_correction=mean_correction)
     L = _native.lib()
     res = {"out": out}
     dev = q.device
@@ -215,7 +222,10 @@ def prefill_workspace_bytes(q, k, v, **kw) -> int:
                 cu_seqlens=kw.get("cu_seqlens"), max_seqlen=kw.get("max_seqlen"),
                 block_q=kw.get("block_q", 128), block_k=kw.get("block_k", 128),
                 softmax_scale=kw.get("softmax_scale"), mode=kw.get("mode", "threshold"),
-                thresholds=kw.get("thresholds"), log_lambda=kw.get("log_lambda"))
+                thresholds=kw.get("thresholds"), log_lambda=kw.get("log_lambda"),
+                v_always=kw.get("v_always", False), block_table=kw.get("block_table"),
+                kv_layout=kw.get("kv_layout", "pthd"),
+                mean_correction=kw.get("mean_correction", False))
     return int(_native.lib().bsfa_prefill_workspace_size(ctypes.byref(p)))
 
 

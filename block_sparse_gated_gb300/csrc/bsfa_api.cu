@@ -2,6 +2,8 @@
 // descriptors, the scheduling pre-pass and the calibration selection kernel.
 // The C ABI is declared in include/bsfa.h.
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -132,6 +134,49 @@ __global__ void __launch_bounds__(1024) select_kernel(const SelectArgs a) {
   }
 }
 
+// ------------------------------------------------------------ block means (mean correction)
+// One CTA per 128-row query tile of the schedule (with Bq = Bk = 128 that is
+// one key block), blockDim = {d, KV heads}: thread (e, h) averages element e
+// of the block's keys and values of KV head h in fp32 and stores the means in
+// the element type at row seqinfo.z + I of the tables [Hkv][rows][d] (the
+// same row numbering as the kept-block bitmap).
+template <bool F16>
+__global__ void __launch_bounds__(1024)
+    block_mean_kernel(const uint16_t* k, const uint16_t* v, long long k_sb, long long k_sh,
+                      long long k_st, long long v_sb, long long v_sh, long long v_st,
+                      const int4* seqinfo, const int2* tiles, const int* ntot, uint16_t* kbar,
+                      uint16_t* vbar, int rows) {
+  if (static_cast<int>(blockIdx.x) >= *ntot) return;
+  const int2 t = tiles[blockIdx.x];
+  const int4 si = seqinfo[t.x];
+  const int e = threadIdx.x, h = threadIdx.y, d = blockDim.x;
+  const int r0 = t.y * TILE, r1 = min(r0 + TILE, si.y);
+  const uint16_t* kp = k + (long long)si.w * k_sb + (long long)h * k_sh + e;
+  const uint16_t* vp = v + (long long)si.w * v_sb + (long long)h * v_sh + e;
+  float sk = 0.f, sv = 0.f;
+#pragma unroll 8
+  for (int r = r0; r < r1; ++r) {
+    const long long tok = si.x + r;
+    const uint16_t a = kp[tok * k_st], b = vp[tok * v_st];
+    if (F16) {
+      sk += __half2float(__ushort_as_half(a));
+      sv += __half2float(__ushort_as_half(b));
+    } else {
+      sk += __bfloat162float(__ushort_as_bfloat16(a));
+      sv += __bfloat162float(__ushort_as_bfloat16(b));
+    }
+  }
+  const float inv = 1.f / static_cast<float>(r1 - r0);
+  const long long o = ((long long)h * rows + si.z + t.y) * d + e;
+  if (F16) {
+    kbar[o] = __half_as_ushort(__float2half_rn(sk * inv));
+    vbar[o] = __half_as_ushort(__float2half_rn(sv * inv));
+  } else {
+    kbar[o] = __bfloat16_as_ushort(__float2bfloat16_rn(sk * inv));
+    vbar[o] = __bfloat16_as_ushort(__float2bfloat16_rn(sv * inv));
+  }
+}
+
 // ------------------------------------------------------------ hang-guard self test
 // One warp waits, through the attention kernel's own bounded-wait helper, on
 // an mbarrier that nothing ever arrives on.  The wait gives up after
@@ -200,35 +245,41 @@ static unsigned* error_word() {
   return static_cast<unsigned*>(ptr);
 }
 
-template <bool CALIB, bool F16, bool G, bool VA, bool PG>
+template <bool CALIB, bool F16, bool G, bool VA, bool PG, bool CR>
 static cudaError_t dispatch_dn(int d, int nq, const Maps& m, const DevParams& p, int grid,
                                cudaStream_t st) {
-  if (d == 128) return nq == 2 ? launch_fwd<128, 2, G, CALIB, F16, VA, PG>(m, p, grid, st)
-                               : launch_fwd<128, 1, G, CALIB, F16, VA, PG>(m, p, grid, st);
-  return nq == 2 ? launch_fwd<64, 2, G, CALIB, F16, VA, PG>(m, p, grid, st)
-                 : launch_fwd<64, 1, G, CALIB, F16, VA, PG>(m, p, grid, st);
+  if (d == 128) return nq == 2 ? launch_fwd<128, 2, G, CALIB, F16, VA, PG, CR>(m, p, grid, st)
+                               : launch_fwd<128, 1, G, CALIB, F16, VA, PG, CR>(m, p, grid, st);
+  return nq == 2 ? launch_fwd<64, 2, G, CALIB, F16, VA, PG, CR>(m, p, grid, st)
+                 : launch_fwd<64, 1, G, CALIB, F16, VA, PG, CR>(m, p, grid, st);
 }
 
+struct Variant {
+  bool gating, vall, paged, corr;
+};
+
 template <bool CALIB, bool F16>
-static cudaError_t dispatch_t(int d, int nq, bool gating, bool vall, bool paged, const Maps& m,
-                              const DevParams& p, int grid, cudaStream_t st) {
+static cudaError_t dispatch_t(int d, int nq, Variant v, const Maps& m, const DevParams& p,
+                              int grid, cudaStream_t st) {
   if constexpr (CALIB) {
-    return dispatch_dn<true, F16, true, false, false>(d, nq, m, p, grid, st);
+    return dispatch_dn<true, F16, true, false, false, false>(d, nq, m, p, grid, st);
   } else {
-    if (paged)
-      return gating ? dispatch_dn<false, F16, true, false, true>(d, nq, m, p, grid, st)
-                    : dispatch_dn<false, F16, false, false, true>(d, nq, m, p, grid, st);
-    if (gating && vall) return dispatch_dn<false, F16, true, true, false>(d, nq, m, p, grid, st);
-    return gating ? dispatch_dn<false, F16, true, false, false>(d, nq, m, p, grid, st)
-                  : dispatch_dn<false, F16, false, false, false>(d, nq, m, p, grid, st);
+    if (v.corr) return dispatch_dn<false, F16, true, false, false, true>(d, nq, m, p, grid, st);
+    if (v.paged)
+      return v.gating ? dispatch_dn<false, F16, true, false, true, false>(d, nq, m, p, grid, st)
+                      : dispatch_dn<false, F16, false, false, true, false>(d, nq, m, p, grid, st);
+    if (v.gating && v.vall)
+      return dispatch_dn<false, F16, true, true, false, false>(d, nq, m, p, grid, st);
+    return v.gating ? dispatch_dn<false, F16, true, false, false, false>(d, nq, m, p, grid, st)
+                    : dispatch_dn<false, F16, false, false, false, false>(d, nq, m, p, grid, st);
   }
 }
 
 template <bool CALIB>
-static cudaError_t dispatch(bool f16, int d, int nq, bool gating, bool vall, bool paged,
-                            const Maps& m, const DevParams& p, int grid, cudaStream_t st) {
-  return f16 ? dispatch_t<CALIB, true>(d, nq, gating, vall, paged, m, p, grid, st)
-             : dispatch_t<CALIB, false>(d, nq, gating, vall, paged, m, p, grid, st);
+static cudaError_t dispatch(bool f16, int d, int nq, Variant v, const Maps& m,
+                            const DevParams& p, int grid, cudaStream_t st) {
+  return f16 ? dispatch_t<CALIB, true>(d, nq, v, m, p, grid, st)
+             : dispatch_t<CALIB, false>(d, nq, v, m, p, grid, st);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -239,11 +290,15 @@ struct Carve {
   int2* tiles;
   int* ntot;
   float* blockmax;
+  uint16_t* kbar;
+  uint16_t* vbar;
   size_t bytes;
 };
 
-// Workspace layout: seqinfo | tiles | ntot | (calibration) blockmax.
-static Carve carve(void* base, int batch, int max_tiles_total, size_t blockmax_elems) {
+// Workspace layout: seqinfo | tiles | ntot | (calibration) blockmax |
+// (mean correction) key means | value means, each [Hkv][rows][d] 16-bit.
+static Carve carve(void* base, int batch, int max_tiles_total, size_t blockmax_elems,
+                   size_t mean_elems = 0) {
   Carve c{};
   size_t off = 0;
   uint8_t* b = static_cast<uint8_t*>(base);
@@ -255,6 +310,10 @@ static Carve carve(void* base, int batch, int max_tiles_total, size_t blockmax_e
   off = align_up(off + sizeof(int), 256);
   c.blockmax = reinterpret_cast<float*>(b + off);
   off = align_up(off + sizeof(float) * blockmax_elems, 256);
+  c.kbar = reinterpret_cast<uint16_t*>(b + off);
+  off = align_up(off + sizeof(uint16_t) * mean_elems, 256);
+  c.vbar = reinterpret_cast<uint16_t*>(b + off);
+  off = align_up(off + sizeof(uint16_t) * mean_elems, 256);
   c.bytes = off;
   return c;
 }
@@ -268,6 +327,16 @@ static long long tiles_bound(const bsfa_fwd_params* p) {
   return (long long)p->batch * ((p->seqlen + TILE - 1) / TILE);
 }
 
+static bool corr_on(const bsfa_fwd_params* p) {
+  return (p->flags & BSFA_FLAG_MEAN_CORRECTION) != 0;
+}
+
+// Elements of one block-mean table (mean correction), 0 when it is off.
+static size_t mean_elems(const bsfa_fwd_params* p) {
+  if (!corr_on(p) || p->num_heads_kv <= 0 || p->head_dim <= 0) return 0;
+  return (size_t)p->num_heads_kv * (size_t)tiles_bound(p) * (size_t)p->head_dim;
+}
+
 static bsfa_status validate(const bsfa_fwd_params* p) {
   if (p == nullptr) return BSFA_ERR_INVALID_ARG;
   if (p->batch < 0 || p->seqlen < 0) return BSFA_ERR_INVALID_ARG;
@@ -275,13 +344,22 @@ static bsfa_status validate(const bsfa_fwd_params* p) {
     return BSFA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return BSFA_ERR_UNSUPPORTED;
   if (p->dtype != BSFA_DTYPE_BF16 && p->dtype != BSFA_DTYPE_F16) return BSFA_ERR_UNSUPPORTED;
-  if (p->flags & ~static_cast<unsigned>(BSFA_FLAG_V_ALWAYS)) return BSFA_ERR_UNSUPPORTED;
+  if (p->flags & ~static_cast<unsigned>(BSFA_FLAG_V_ALWAYS | BSFA_FLAG_MEAN_CORRECTION))
+    return BSFA_ERR_UNSUPPORTED;
   if ((p->block_q != 64 && p->block_q != 128) || (p->block_k != 64 && p->block_k != 128))
     return BSFA_ERR_UNSUPPORTED;
   if (p->mode < BSFA_GATE_THRESHOLD || p->mode > BSFA_GATE_NONE) return BSFA_ERR_INVALID_ARG;
   if (p->batch > MAX_BATCH) return BSFA_ERR_UNSUPPORTED;
   if (p->cu_seqlens && p->seqlen > 0 && p->max_seqlen <= 0) return BSFA_ERR_INVALID_ARG;
   if ((max_len_of(p) + TILE - 1) / TILE > MAX_TILES_PER_SEQ) return BSFA_ERR_UNSUPPORTED;
+  if (corr_on(p)) {
+    // Stand-ins need gating, 128 x 128 blocks (one key block per tile),
+    // contiguous K/V and at most 32 * CORR_WORDS candidate blocks per row.
+    if (p->mode == BSFA_GATE_NONE || p->block_q != TILE || p->block_k != TILE ||
+        p->block_table != nullptr || (p->flags & BSFA_FLAG_V_ALWAYS) ||
+        (max_len_of(p) + TILE - 1) / TILE > 32 * CORR_WORDS)
+      return BSFA_ERR_UNSUPPORTED;
+  }
   if (p->batch == 0 || p->seqlen == 0) return BSFA_OK;
   if (!p->q || !p->k || !p->v || !p->o) return BSFA_ERR_INVALID_ARG;
   if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->o))
@@ -332,7 +410,7 @@ const char* bsfa_status_string(bsfa_status s) {
 size_t bsfa_prefill_workspace_size(const bsfa_fwd_params* p) {
   if (p == nullptr || p->batch < 0 || p->seqlen < 0 || p->batch > MAX_BATCH) return 0;
   if (p->cu_seqlens != nullptr && p->max_seqlen < 0) return 0;
-  return carve(nullptr, p->batch, (int)tiles_bound(p), 0).bytes;
+  return carve(nullptr, p->batch, (int)tiles_bound(p), 0, mean_elems(p)).bytes;
 }
 
 bsfa_status bsfa_bitmap_words_per_row(const bsfa_fwd_params* p, int* words_per_row) {
@@ -348,8 +426,9 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   if (p->batch == 0 || p->seqlen == 0) return BSFA_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const long long tb = tiles_bound(p);
-  const Carve cv = carve(p->workspace, p->batch, (int)tb, 0);
+  const Carve cv = carve(p->workspace, p->batch, (int)tb, 0, mean_elems(p));
   if (p->workspace_bytes < cv.bytes) return BSFA_ERR_WORKSPACE;
+  const bool corr = corr_on(p);
 
   const int d = p->head_dim;
   const int g = p->num_heads_q / p->num_heads_kv;
@@ -381,6 +460,17 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
              !make_map(&m.v, p->v, f16, d, p->seqlen, p->num_heads_kv, bdim, p->v_stride[2],
                        p->v_stride[1], bstride(p->v_stride, p->num_heads_kv))) {
     return BSFA_ERR_CUDA;
+  }
+  m.kb = m.k;
+  m.vb = m.v;
+  if (corr) {
+    // Block-mean tables [Hkv][tb][d]: row r is key block r of the bitmap's
+    // row numbering.
+    if (!make_map(&m.kb, cv.kbar, f16, d, tb, p->num_heads_kv, 1, d, tb * d,
+                  tb * d * p->num_heads_kv) ||
+        !make_map(&m.vb, cv.vbar, f16, d, tb, p->num_heads_kv, 1, d, tb * d,
+                  tb * d * p->num_heads_kv))
+      return BSFA_ERR_CUDA;
   }
 
   DevParams dp{};
@@ -415,6 +505,7 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   dp.btab = paged ? p->block_table : nullptr;
   dp.bt_stride = paged ? p->block_table_stride : 0;
   dp.tiles_per_page = paged ? p->page_size / TILE : 1;
+  dp.corr_shift = std::log(static_cast<float>(p->block_k)) / dp.sigma;
   dp.err = error_word();
   if (dp.err == nullptr) return BSFA_ERR_CUDA;
 
@@ -428,13 +519,29 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
                                                        cv.seqinfo, cv.tiles, cv.ntot,
                                                        p->block_counts);
   if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;
+  if (corr) {
+    const dim3 mb_block(d, p->num_heads_kv);
+    if (d * p->num_heads_kv > 1024) return BSFA_ERR_UNSUPPORTED;
+    const auto* kk = static_cast<const uint16_t*>(p->k);
+    const auto* vv = static_cast<const uint16_t*>(p->v);
+    const long long ksb = varlen ? 0 : p->k_stride[0], vsb = varlen ? 0 : p->v_stride[0];
+    if (f16)
+      block_mean_kernel<true><<<(unsigned)tb, mb_block, 0, stream>>>(
+          kk, vv, ksb, p->k_stride[1], p->k_stride[2], vsb, p->v_stride[1], p->v_stride[2],
+          cv.seqinfo, cv.tiles, cv.ntot, cv.kbar, cv.vbar, (int)tb);
+    else
+      block_mean_kernel<false><<<(unsigned)tb, mb_block, 0, stream>>>(
+          kk, vv, ksb, p->k_stride[1], p->k_stride[2], vsb, p->v_stride[1], p->v_stride[2],
+          cv.seqinfo, cv.tiles, cv.ntot, cv.kbar, cv.vbar, (int)tb);
+    if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;
+  }
   const long long units = tb * p->num_heads_kv * (g / nq);
   const int sms = num_sms();
   if (sms <= 0) return BSFA_ERR_CUDA;
   const int grid = (int)(units < sms ? units : sms);
   const bool vall = (p->flags & BSFA_FLAG_V_ALWAYS) != 0;
-  if (dispatch<false>(f16, d, nq, p->mode != BSFA_GATE_NONE, vall, paged, m, dp, grid, stream) !=
-      cudaSuccess)
+  const Variant var{p->mode != BSFA_GATE_NONE, vall, paged, corr};
+  if (dispatch<false>(f16, d, nq, var, m, dp, grid, stream) != cudaSuccess)
     return BSFA_ERR_CUDA;
   return BSFA_OK;
 }
@@ -532,8 +639,9 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
         !make_map(&m.k, k_samples[n], f16, d, L, Hkv, 1, k_stride[1], k_stride[0],
                   (long long)k_stride[0] * Hkv))
       return BSFA_ERR_CUDA;
-    m.v = m.k;
-    if (dispatch<true>(f16, d, nq, true, false, false, m, dp, grid, stream) != cudaSuccess)
+    m.v = m.kb = m.vb = m.k;
+    if (dispatch<true>(f16, d, nq, Variant{true, false, false, false}, m, dp, grid, stream) !=
+        cudaSuccess)
       return BSFA_ERR_CUDA;
     sa.sample = n;
     select_kernel<<<dim3(nqb, Hq), sel_threads, sel_smem, stream>>>(sa);

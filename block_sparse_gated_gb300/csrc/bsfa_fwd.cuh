@@ -32,6 +32,10 @@ namespace bsfa {
 
 constexpr int TILE = 128;
 constexpr int KST = 2;  // K ring stages
+// Mean correction: words of kept-candidate bits kept per softmax warp (one
+// bit per candidate key block), so sequences of up to 32 * CORR_WORDS * 128
+// = 512K tokens.
+constexpr int CORR_WORDS = 128;
 constexpr int VST = 2;  // V ring stages
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -82,6 +86,9 @@ struct DevParams {
   // J % tiles_per_page (a 128-key tile never straddles two pages).
   const int* btab;
   int bt_stride, tiles_per_page;
+  // Mean correction: ln(Bk) / sigma, the stand-in logit's shift in the raw
+  // score units the kernel keeps its maxima in.
+  float corr_shift;
   unsigned* err;
 };
 
@@ -117,7 +124,7 @@ struct Ctrl {
   int abort;
 };
 
-template <int D, int NQ, bool CALIB>
+template <int D, int NQ, bool CALIB, bool CORR = false>
 struct Layout {
   static constexpr int TB = TILE * D * 2;  // bytes of one 128-row bf16 tile
   static constexpr int NV = CALIB ? 0 : VST;
@@ -127,7 +134,10 @@ struct Layout {
   static constexpr int C_OFF = V_OFF + NV * TB;
   // + alignment slack; at least 120 KB so that a single CTA is resident per SM
   // (the persistent grid assumes it and the TMEM allocation is not shared).
-  static constexpr int RAW = C_OFF + (int)sizeof(Ctrl<D, NQ>) + 1024;
+  // Mean correction: kept-candidate bit words, [slot][warp][CORR_WORDS].
+  static constexpr int KB_OFF = C_OFF + (((int)sizeof(Ctrl<D, NQ>) + 15) & ~15);
+  static constexpr int KB_BYTES = CORR ? NQ * 4 * CORR_WORDS * 4 : 0;
+  static constexpr int RAW = KB_OFF + KB_BYTES + 1024;
   static constexpr int BYTES = RAW > 120 * 1024 ? RAW : 120 * 1024;
   static constexpr int NCOLS = (NQ * 128 + NQ * D) <= 256 ? 256 : 512;
   static constexpr int NTHREADS = 128 + 128 * NQ;
@@ -267,12 +277,19 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 
 // VALL (gated only): load V for every visible tile, kept or not.
 // PAGED: K and V come from page pools through the block table.
-template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
-__global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
+// CORR (gated, Bq = Bk = 128): mean correction.  After a unit's key tiles,
+// ceil(I / 128) correction tiles run through the same pipeline: their "keys"
+// and "values" are the block means of 128 consecutive key blocks (tmKb,
+// tmVb), and only the blocks this slot skipped enter them, with the logit
+// shifted by ln(Bk) so that one mean stands for the block's Bk keys.
+template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED, bool CORR>
+__global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
     bsfa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const DevParams p) {
-  using LY = Layout<D, NQ, CALIB>;
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmKb,
+                    const __grid_constant__ CUtensorMap tmVb, const DevParams p) {
+  using LY = Layout<D, NQ, CALIB, CORR>;
   constexpr int TB = LY::TB;
   constexpr int HALF = TILE * 128;  // bytes of one 64-column swizzled half
   constexpr int NHALF = D / 64;
@@ -283,6 +300,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
   uint8_t* sK = base + LY::K_OFF;
   uint8_t* sV = base + LY::V_OFF;
   Ctrl<D, NQ>* c = reinterpret_cast<Ctrl<D, NQ>*>(base + LY::C_OFF);
+  uint32_t* kbits = reinterpret_cast<uint32_t*>(base + LY::KB_OFF);  // CORR only
   volatile int* abort = &c->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -354,6 +372,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       const int pr = rem % p.pairs;
       const int4 si = p.seqinfo[t.x];
       const int I = t.y, nkt = I + 1;
+      const int ntt = nkt + (CORR ? (I + TILE - 1) / TILE : 0);  // + correction tiles
       const int row0 = si.x + I * TILE;
       if (!(ok = wait_all(&c->q_empty, (uc & 1) ^ 1, abort, p.err, ERR_WAIT_Q_EMPTY))) break;
       if (elect_one()) {
@@ -366,19 +385,25 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       }
       __syncwarp();
       last_q = static_cast<int>(uc);
-      for (int J = -1; J < nkt; ++J) {
+      for (int J = -1; J < ntt; ++J) {
         // K for tile J + 1 (tile 0 before the loop proper), then V for tile J.
-        if (J + 1 < nkt) {
+        if (J + 1 < ntt) {
           const uint32_t st = kc % KST;
           if (!(ok = wait_all(&c->k_empty[st], ((kc / KST) & 1) ^ 1, abort, p.err,
                               ERR_WAIT_K_EMPTY)))
             break;
           if (elect_one()) {
-            const int2 kc2 = kv_tile_coord<PAGED>(p, si, t.x, J + 1);
             mbar_arrive_expect_tx(&c->k_full[st], TB);
-            for (int hf = 0; hf < NHALF; ++hf)
-              tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64, kc2.x, kvh,
-                          kc2.y);
+            if (!CORR || J + 1 < nkt) {
+              const int2 kc2 = kv_tile_coord<PAGED>(p, si, t.x, J + 1);
+              for (int hf = 0; hf < NHALF; ++hf)
+                tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64, kc2.x, kvh,
+                            kc2.y);
+            } else {  // block means of key blocks [128 (J + 1 - nkt), +128)
+              for (int hf = 0; hf < NHALF; ++hf)
+                tma_load_4d(sK + st * TB + hf * HALF, &tmKb, &c->k_full[st], hf * 64,
+                            si.z + (J + 1 - nkt) * TILE, kvh, 0);
+            }
           }
           __syncwarp();
           ++kc;
@@ -428,7 +453,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       const int2 t = p.tiles[rem / p.pairs];
       const int4 si = p.seqinfo[t.x];
       const int nkt = t.y + 1;
-      for (int J = 0; J < nkt; ++J, ++tc) {
+      const int ntt = nkt + (CORR ? (t.y + TILE - 1) / TILE : 0);
+      for (int J = 0; J < ntt; ++J, ++tc) {
         // Every slot's decision is read on every tile (V is issued on the
         // first one that keeps the tile), so this warp consumes each
         // decision phase in order instead of skipping some.  With VALL no
@@ -449,11 +475,17 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                               ERR_WAIT_V_EMPTY)))
             break;
           if (elect_one()) {
-            const int2 vc2 = kv_tile_coord<PAGED>(p, si, t.x, J);
             mbar_arrive_expect_tx(&c->v_full[st], TB);
-            for (int hf = 0; hf < NHALF; ++hf)
-              tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64, vc2.x, kvh,
-                          vc2.y);
+            if (!CORR || J < nkt) {
+              const int2 vc2 = kv_tile_coord<PAGED>(p, si, t.x, J);
+              for (int hf = 0; hf < NHALF; ++hf)
+                tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64, vc2.x, kvh,
+                            vc2.y);
+            } else {  // value means of key blocks [128 (J - nkt), +128)
+              for (int hf = 0; hf < NHALF; ++hf)
+                tma_load_4d(sV + st * TB + hf * HALF, &tmVb, &c->v_full[st], hf * 64,
+                            si.z + (J - nkt) * TILE, kvh, 0);
+            }
           }
           __syncwarp();
           ++vc;
@@ -486,6 +518,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
       const int2 t = p.tiles[(u % per_kv) / p.pairs];
       const int nkt = t.y + 1;
+      const int ntt = nkt + (CORR ? (t.y + TILE - 1) / TILE : 0);
       for (int s = 0; s < NQ && ok; ++s)
         ok = wait_all(&c->q_full[s], uc & 1, abort, p.err, ERR_WAIT_Q_FULL);
       if (!ok) break;
@@ -498,13 +531,13 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             umma_commit(&c->s_full[s]);
           }
           umma_commit(&c->k_empty[st]);
-          if (nkt == 1) umma_commit(&c->q_empty);
+          if (ntt == 1) umma_commit(&c->q_empty);
         }
         __syncwarp();
         ++kc;
       }
       uint32_t first_mask = (1u << NQ) - 1u;  // slots whose O has not been written yet
-      for (int J = 0; J < nkt && ok; ++J, ++tc) {
+      for (int J = 0; J < ntt && ok; ++J, ++tc) {
         const int tb = tc & 1;
         const uint32_t vst = vc % VST;
         const uint32_t kst = kc % KST;
@@ -512,7 +545,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
         for (int s = 0; s < NQ; ++s) {
           bool do_pv = false;
           uint32_t acc = 1u;
-          const bool do_qk = J + 1 < nkt;
+          const bool do_qk = J + 1 < ntt;
           const uint32_t ppar = (tc >> 1) & 1u;
           // Every shared-memory access of this warp queues behind the
           // operand reads of the MMAs it has just issued (Q.K^T reads both
@@ -590,7 +623,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
               umma_commit(&c->s_full[s]);
               if (s == NQ - 1) {
                 umma_commit(&c->k_empty[kst]);
-                if (J + 1 == nkt - 1) umma_commit(&c->q_empty);
+                if (J + 1 == ntt - 1) umma_commit(&c->q_empty);
               }
             }
           }
@@ -671,9 +704,28 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
       int bm_idx = 0;
       const bool bm_on = (p.bitmap != nullptr) && lead_warp && (my_i * p.Bq < len);
       const long long bm_row = ((long long)(si.z + my_i) * p.Hq + h) * (long long)p.words;
+      // Mean correction (Bq = Bk = 128: the candidates of query block I are
+      // key blocks 0 .. I-1): kept bits of the candidates, one word per 32
+      // blocks, in this warp's own shared-memory row.
+      const int ntt = nkt + (CORR ? (I + TILE - 1) / TILE : 0);
+      uint32_t* my_kbits = kbits + (s * 4 + wq) * CORR_WORDS;
+      uint32_t kbit_acc = 0;
 
-      for (int J = 0; J < nkt; ++J, ++tc) {
+      for (int J = 0; J < ntt; ++J, ++tc) {
         const int tb = tc & 1;
+        const bool corr_tile = CORR && J >= nkt;  // block means, not keys
+        // Correction tile: entry e stands for key block jb + e, which enters
+        // iff it is a candidate (jb + e < I) that this slot skipped.
+        uint32_t inc[4] = {0u, 0u, 0u, 0u};
+        if (corr_tile) {
+          const int jb = (J - nkt) * TILE;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int lim = I - jb - 32 * q;
+            const uint32_t cand = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
+            inc[q] = cand & ~my_kbits[(jb >> 5) + q];
+          }
+        }
         const uint32_t ph = (tc >> 1) & 1u;  // phase parity of the per-tile-parity barriers
         // Waits here are bounded.  In the gated kernel every thread joins the
         // per-tile vote barrier even after its own wait gave up, and the
@@ -698,7 +750,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
           tmem_wait_ld();
-          if (!diag_tile) {
+          if (corr_tile) {
+#pragma unroll
+            for (int e = 0; e < 128; ++e)
+              if ((inc[e >> 5] >> (e & 31)) & 1u) rm0 = fmaxf(rm0, __uint_as_float(sr[e >> 5][e & 31]));
+            rm1 = rm0;
+          } else if (!diag_tile) {
             rm0 = max3f(__uint_as_float(sr[0][0]), __uint_as_float(sr[0][1]),
                         __uint_as_float(sr[0][2]));
             rm1 = max3f(__uint_as_float(sr[2][0]), __uint_as_float(sr[2][1]),
@@ -793,7 +850,13 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             // fence orders it before the barrier, so that the MMA warp may
             // overwrite S as soon as it reads a skip decision.
             tc_fence_before();
-            if (simple) {
+            if (corr_tile) {
+              // Kept iff some block of the range was skipped (the same for
+              // every thread); the barrier only keeps the warpgroup together.
+              ok = bar_red_and(bar_id, 128, okl);
+              if (!ok) break;
+              keep[0][0] = (inc[0] | inc[1] | inc[2] | inc[3]) != 0u;
+            } else if (simple) {
               // One 128x128 semantic block per tile: the hardware barrier
               // itself carries the vote (no shared-memory traffic, which
               // queues behind the MMAs' operand reads).  Lane 0 of each warp
@@ -821,7 +884,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
                 if (cls[1][k] == 1) keep[1][k] = (vq1 >> k) & 1u;
               }
             }
-            if (lambda_mode) {
+            if (lambda_mode && !corr_tile) {
               // Sub-blocks in ascending key order; a row's running max moves
               // only with the blocks it keeps, so the second key half is voted
               // on after the first half's decision.
@@ -862,8 +925,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             const bool k0 = (myqs ? keep[1][0] : keep[0][0]);
             const bool k1 = (KS == 1) ? k0 : (myqs ? keep[1][1] : keep[0][1]);
             float rmk = -CUDART_INF_F;
-            if (k0) rmk = fmaxf(rmk, rm0);
-            if (k1) rmk = fmaxf(rmk, rm1);
+            // A stand-in's logit carries ln(Bk): one mean weighs Bk keys.
+            if (k0) rmk = fmaxf(rmk, corr_tile ? rm0 + p.corr_shift : rm0);
+            if (k1) rmk = fmaxf(rmk, corr_tile ? rm1 + p.corr_shift : rm1);
             const float m_new = fmaxf(m_used, rmk);
             const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
             float alpha = 1.f;
@@ -890,8 +954,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
             // columns have been read by then).
             const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * sc;
             const uint64_t sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
+            const float bias = corr_tile ? p.corr_shift * sc - mb : -mb;
             uint64_t lsum2 = f2_pack(0.f, 0.f);
-            const bool fast = !diag_tile && k0 && k1;
+            const bool fast = !diag_tile && k0 && k1 && !corr_tile;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               const bool kk = (hf == 0) ? k0 : k1;
@@ -917,12 +982,14 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                   const int cc = hf * 64 + 2 * e;
-                  const bool vis0 = kk && !(diag_tile && cc > row);
-                  const bool vis1 = kk && !(diag_tile && cc + 1 > row);
+                  const bool vis0 = corr_tile ? ((inc[cc >> 5] >> (cc & 31)) & 1u) != 0u
+                                              : kk && !(diag_tile && cc > row);
+                  const bool vis1 = corr_tile ? ((inc[(cc + 1) >> 5] >> ((cc + 1) & 31)) & 1u) != 0u
+                                              : kk && !(diag_tile && cc + 1 > row);
                   const float x0 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e) & 31]);
                   const float x1 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e + 1) & 31]);
-                  const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
-                  const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
+                  const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, bias)) : 0.f;
+                  const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, bias)) : 0.f;
                   lsum2 = f2_add(lsum2, f2_pack(p0, p1));
                   pk[e] = pack_x2<F16>(p0, p1);
                 }
@@ -940,7 +1007,16 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB>::NTHREADS, 1)
 
           // ---- bookkeeping: bitmap words and block counts (after the
           // hand-off of P, off the path to the next MMA)
-          if (lead_warp && my_i * p.Bq < len) {
+          if constexpr (CORR) {
+            if (J < I) {  // a candidate: record whether this slot kept it
+              kbit_acc |= (keep[0][0] ? 1u : 0u) << (J & 31);
+              if ((J & 31) == 31 || J == I - 1) {
+                my_kbits[J >> 5] = kbit_acc;  // every lane: same value
+                kbit_acc = 0u;
+              }
+            }
+          }
+          if (!corr_tile && lead_warp && my_i * p.Bq < len) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               const int cl = (myqs ? cls[1][k] : cls[0][k]);

@@ -10,10 +10,11 @@ namespace bsfa {
 
 struct Maps {
   CUtensorMap q, k, v;
+  CUtensorMap kb, vb;  // block-mean tables (mean correction); copies of k, v otherwise
 };
 
-// Launches bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL, PAGED> with its shared-memory size.
-template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
+// Launches bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL, PAGED, CORR> with its shared-memory size.
+template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED, bool CORR>
 cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream);
 
 }  // namespace bsfa

@@ -4,10 +4,10 @@
 
 namespace bsfa {
 
-template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
+template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED, bool CORR>
 cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream) {
-  using LY = Layout<D, NQ, CALIB>;
-  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL, PAGED>;
+  using LY = Layout<D, NQ, CALIB, CORR>;
+  auto* fn = &bsfa_fwd_kernel<D, NQ, GATING, CALIB, F16, VALL, PAGED, CORR>;
   static bool configured[64] = {};  // the attribute is per device; set once on each
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -27,14 +27,16 @@ cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t
     }
     if (dev < 64) configured[dev] = true;
   }
-  fn<<<grid, LY::NTHREADS, LY::BYTES, stream>>>(m.q, m.k, m.v, p);
+  fn<<<grid, LY::NTHREADS, LY::BYTES, stream>>>(m.q, m.k, m.v, m.kb, m.vb, p);
   return cudaGetLastError();
 }
 
 }  // namespace bsfa
 
-#define BSFA_INSTANTIATE(D, NQ, G, C, F) BSFA_INSTANTIATE_VP(D, NQ, G, C, F, false, false)
-#define BSFA_INSTANTIATE_V(D, NQ, G, C, F, VA) BSFA_INSTANTIATE_VP(D, NQ, G, C, F, VA, false)
-#define BSFA_INSTANTIATE_VP(D, NQ, G, C, F, VA, PG)                                          \
-  template cudaError_t bsfa::launch_fwd<D, NQ, G, C, F, VA, PG>(const Maps&, const DevParams&, \
-                                                               int, cudaStream_t);
+#define BSFA_INSTANTIATE(D, NQ, G, C, F) BSFA_INSTANTIATE_X(D, NQ, G, C, F, false, false, false)
+#define BSFA_INSTANTIATE_V(D, NQ, G, C, F, VA) BSFA_INSTANTIATE_X(D, NQ, G, C, F, VA, false, false)
+#define BSFA_INSTANTIATE_VP(D, NQ, G, C, F, VA, PG) BSFA_INSTANTIATE_X(D, NQ, G, C, F, VA, PG, false)
+#define BSFA_INSTANTIATE_X(D, NQ, G, C, F, VA, PG, CR)                                  \
+  template cudaError_t bsfa::launch_fwd<D, NQ, G, C, F, VA, PG, CR>(const Maps&,        \
+                                                                    const DevParams&, int, \
+                                                                    cudaStream_t);

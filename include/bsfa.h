@@ -86,7 +86,19 @@ typedef enum {
    * still loaded" in its discussion of skipped blocks); skipped tiles still
    * get no exp, no P.V and no m/l/O update, so results are bit-identical to
    * flags = 0.  Exists to measure what skipping the V load saves. */
-  BSFA_FLAG_V_ALWAYS = 1
+  BSFA_FLAG_V_ALWAYS = 1,
+  /* THRESHOLD and LAMBDA modes: mean correction for skipped blocks ("FlashPrefill
+   * V2" summary, agihunt.info, mean correction).  Every skipped candidate block J
+   * of a query block enters that block's softmax through a zero-order stand-in:
+   * with the block's mean key kbar_J and mean value vbar_J, each row adds the
+   * weight Bk * exp(sigma * q . kbar_J) to the denominator and that weight times
+   * vbar_J to the numerator.  The gate's decisions, the bitmap and the counts are
+   * unchanged.  The block means are computed in fp32 from K and V and stored in
+   * the element type in the workspace (bsfa_prefill_workspace_size includes
+   * them).  Requires block_q == block_k == 128, contiguous K/V (block_table
+   * NULL), no BSFA_FLAG_V_ALWAYS and sequences of at most 524288 tokens; else
+   * BSFA_ERR_UNSUPPORTED. */
+  BSFA_FLAG_MEAN_CORRECTION = 2
 } bsfa_flag;
 
 /*

@@ -68,7 +68,7 @@ def test_host_side_validation_without_gpu(libpath):
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unsupported block size
     p.block_k, p.dtype = 128, 7
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unknown element type
-    p.dtype, p.flags = _native.DTYPE_F16, 2
+    p.dtype, p.flags = _native.DTYPE_F16, 4
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unknown flag bit
     p.flags = _native.FLAG_V_ALWAYS
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # null tensors
@@ -132,6 +132,34 @@ def test_paged_parameters_are_validated_on_the_host(libpath):
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2
     p.k_stride[0] = 256 * 2 * 128
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 5  # all fine up to the missing workspace
+
+
+def test_mean_correction_parameters_are_validated_on_the_host(libpath):
+    import ctypes
+    from block_sparse_gated_gb300 import _native
+    L = _native.lib()
+    p = _native.FwdParams()
+    p.batch, p.num_heads_q, p.num_heads_kv, p.seqlen, p.head_dim = 1, 4, 2, 1000, 128
+    p.block_q = p.block_k = 128
+    p.mode = 1
+    p.q = p.k = p.v = p.o = 1 << 20  # 16-byte aligned stand-ins, never read
+    p.q_stride[:] = p.o_stride[:] = (4 * 1000 * 128, 1000 * 128, 128)
+    p.k_stride[:] = p.v_stride[:] = (2 * 1000 * 128, 1000 * 128, 128)
+    plain = L.bsfa_prefill_workspace_size(ctypes.byref(p))
+    p.flags = _native.FLAG_MEAN_CORRECTION
+    # the workspace grows by two block-mean tables: 2 KV heads x 8 blocks x 128 x 2 bytes each
+    assert L.bsfa_prefill_workspace_size(ctypes.byref(p)) >= plain + 2 * 2 * 8 * 128 * 2
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 5  # fine up to the missing workspace
+    p.mode = 2
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # nothing is skipped without a gate
+    p.mode, p.block_k = 0, 64
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # 128 x 128 blocks only
+    p.block_k = 128
+    p.flags |= _native.FLAG_V_ALWAYS
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2
+    p.flags = _native.FLAG_MEAN_CORRECTION
+    p.block_table, p.block_table_stride, p.page_size, p.num_pages = 1 << 12, 8, 128, 8
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # contiguous K/V only
 
 
 def test_mixed_element_types_are_rejected_before_the_library():

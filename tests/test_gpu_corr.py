@@ -1,0 +1,124 @@
+"""Mean correction for skipped blocks (the stand-in of the "FlashPrefill V2"
+summary, agihunt.info) on the GPU path, against the fp64 oracle with the same
+option.  The gate's decisions do not depend on it, so the bitmaps are still
+compared bit for bit; outputs and log-sum-exp use the bf16 tolerances."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_gated_gb300 import workloads as wl
+from oracle import bsfa_oracle as orc
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+B = 128
+
+
+def _bsfa():
+    import block_sparse_gated_gb300 as b
+    return b
+
+
+def _run(q, k, v, **kw):
+    b = _bsfa()
+    r = b.prefill(q, k, v, return_bitmap=True, return_lse=True, return_counts=True, **kw)
+    torch.cuda.synchronize()
+    assert b.api.device_error() == 0
+    return r
+
+
+@pytest.mark.parametrize("Hq,Hkv,L,d", [(4, 2, 1000, 128), (2, 1, 777, 64), (1, 1, 640, 128)])
+def test_corrected_threshold_gate_matches_oracle(cuda_device, Hq, Hkv, L, d):
+    x = wl.layer_inputs(Hq, Hkv, L, d, 400 + L, skip_rate=0.4)
+    q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
+    sigma = gu.default_sigma(d)
+    T = gu.median_table(q64, k64, B, B, sigma, jitter_seed=L)
+    T, _, _ = gu.guarded_thresholds(q64, k64, T, B, B, sigma)
+    r = _run(x.q.to(cuda_device)[None], x.k.to(cuda_device)[None], x.v.to(cuda_device)[None],
+             mode="threshold", thresholds=torch.from_numpy(T).to(cuda_device),
+             mean_correction=True)
+    ref = orc.prefill(q64, k64, v64, Bq=B, Bk=B, thresholds=T.astype(np.float64),
+                      mean_correction=True)
+    bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, [L], B, B)
+    assert clean and np.array_equal(bits[0], ref["keep"])
+    assert (~ref["keep"][ref["candidate"]]).sum() > 0  # some blocks were skipped
+    gu.assert_close(gu.to64(r["out"][0]), ref["out"], "out")
+    gu.assert_close(gu.to64(r["lse"]).reshape(Hq, L), ref["lse"], "lse", max_abs=gu.LSE_ABS,
+                    mean_abs=gu.LSE_ABS)
+
+
+def test_corrected_lambda_gate_varlen_matches_oracle(cuda_device):
+    Hq, Hkv, d = 4, 2, 128
+    lens = [300, 1000, 129, 0, 513]
+    parts = [wl.layer_inputs(Hq, Hkv, Ln, d, 420 + n, skip_rate=0.5) if Ln else None
+             for n, Ln in enumerate(lens)]
+    qs = [p.q if p else torch.empty(Hq, 0, d, dtype=torch.bfloat16) for p in parts]
+    ks = [p.k if p else torch.empty(Hkv, 0, d, dtype=torch.bfloat16) for p in parts]
+    vs = [p.v if p else torch.empty(Hkv, 0, d, dtype=torch.bfloat16) for p in parts]
+    q, cu = wl.pack_varlen(qs)
+    k, _ = wl.pack_varlen(ks)
+    v, _ = wl.pack_varlen(vs)
+    r = _bsfa().prefill(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                        cu_seqlens=cu.to(cuda_device), max_seqlen=max(lens), mode="lambda",
+                        log_lambda=-1.0, mean_correction=True, return_bitmap=True,
+                        return_lse=True)
+    torch.cuda.synchronize()
+    assert _bsfa().api.device_error() == 0
+    ref = orc.prefill_varlen(gu.to64(q), gu.to64(k), gu.to64(v), cu.numpy(), Bq=B, Bk=B,
+                             mode="lambda", log_lambda=-1.0, mean_correction=True)
+    bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, lens, B, B)
+    assert clean
+    for n, Ln in enumerate(lens):
+        if Ln:
+            assert np.array_equal(bits[n], ref["keep"][n]), f"sequence {n}"
+    gu.assert_close(gu.to64(r["out"]), ref["out"], "out")
+    gu.assert_close(gu.to64(r["lse"]), ref["lse"], "lse", max_abs=gu.LSE_ABS, mean_abs=gu.LSE_ABS)
+
+
+def test_constant_blocks_make_the_correction_exact(cuda_device):
+    """K and V constant inside every 128-key block: with every candidate
+    skipped (T = +inf), the corrected output equals dense attention."""
+    Hq, Hkv, L, d = 2, 1, 900, 128
+    g = torch.Generator().manual_seed(430)
+    nb = math.ceil(L / B)
+    kb = torch.randn(Hkv, nb, d, generator=g) * 0.5
+    vb = torch.randn(Hkv, nb, d, generator=g)
+    k = kb.repeat_interleave(B, dim=1)[:, :L].to(torch.bfloat16)
+    v = vb.repeat_interleave(B, dim=1)[:, :L].to(torch.bfloat16)
+    q = torch.randn(Hq, L, d, generator=g).to(torch.bfloat16)
+    qd, kd, vd = (t.to(cuda_device)[None] for t in (q, k, v))
+    T = torch.full((Hq, 1), math.inf, device=cuda_device)
+    corr = _run(qd, kd, vd, mode="threshold", thresholds=T, mean_correction=True)
+    dense = _run(qd, kd, vd, mode="none")
+    plain = _run(qd, kd, vd, mode="threshold", thresholds=T)
+    assert int(corr["counts"][0]) == 0  # every candidate skipped
+    gu.assert_close(gu.to64(corr["out"][0]), gu.to64(dense["out"][0]), "corrected vs dense")
+    err_plain = np.abs(gu.to64(plain["out"][0]) - gu.to64(dense["out"][0])).max()
+    assert err_plain > 0.05  # without the stand-ins the outputs differ
+
+
+def test_correction_without_skips_changes_nothing(cuda_device):
+    Hq, Hkv, L, d = 4, 2, 700, 128
+    x = wl.layer_inputs(Hq, Hkv, L, d, 440)
+    q, k, v = (t.to(cuda_device)[None] for t in (x.q, x.k, x.v))
+    T = torch.full((Hq, 1), -math.inf, device=cuda_device)
+    a = _run(q, k, v, mode="threshold", thresholds=T)
+    b = _run(q, k, v, mode="threshold", thresholds=T, mean_correction=True)
+    for key in ("out", "lse", "bitmap", "counts"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_fp16_corrected_matches_oracle(cuda_device):
+    Hq, Hkv, L, d = 2, 2, 600, 64
+    x = wl.layer_inputs(Hq, Hkv, L, d, 450, skip_rate=0.5, dtype=torch.float16)
+    q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
+    r = _run(x.q.to(cuda_device)[None], x.k.to(cuda_device)[None], x.v.to(cuda_device)[None],
+             mode="lambda", log_lambda=-1.0, mean_correction=True)
+    ref = orc.prefill(q64, k64, v64, Bq=B, Bk=B, mode="lambda", log_lambda=-1.0,
+                      mean_correction=True)
+    bits, _ = gu.unpack_bitmap(r["bitmap"], Hq, [L], B, B)
+    assert np.array_equal(bits[0], ref["keep"])
+    gu.assert_close(gu.to64(r["out"][0]), ref["out"], "out", max_abs=4e-3, mean_abs=4e-4)

@@ -71,7 +71,7 @@ def _oracle_rows_T(cal, heads_rows, Bq, Bk, ks, sigma, g):
 
 
 def _check_blocks(hc, blocks, Bq, Bk, sigma, L, bitmap_rows, out, lse, mode, T=None,
-                  log_lambda=None):
+                  log_lambda=None, mean_correction=False):
     """Compare sampled query blocks of one sequence with the oracle."""
     Hq = out.shape[0]
     worst = 0.0
@@ -80,7 +80,7 @@ def _check_blocks(hc, blocks, Bq, Bk, sigma, L, bitmap_rows, out, lse, mode, T=N
         r = orc.query_block(hc.qh(h), hc.kh(h), hc.vh(h), i, Bq=Bq, Bk=Bk, sigma=sigma,
                             mode=mode,
                             T_hi=None if T is None else float(T[h, orc.threshold_index(i, nT)]),
-                            log_lambda=log_lambda)
+                            log_lambda=log_lambda, mean_correction=mean_correction)
         words = bitmap_rows[i, h].astype(np.uint32)
         for j, kept in r["keep"].items():
             bit = bool((int(words[j >> 5]) >> (j & 31)) & 1)
@@ -95,7 +95,7 @@ def _check_blocks(hc, blocks, Bq, Bk, sigma, L, bitmap_rows, out, lse, mode, T=N
     return worst
 
 
-def _threshold_case(dev, name, k_index=0):
+def _threshold_case(dev, name, k_index=0, mean_correction=False):
     cfg = wl.WORKLOADS[name]
     Hq, Hkv, d, Bq, Bk, L = (cfg[x] for x in ("Hq", "Hkv", "d", "Bq", "Bk", "L"))
     g, sigma = Hq // Hkv, 1.0 / math.sqrt(d)
@@ -139,12 +139,13 @@ def _threshold_case(dev, name, k_index=0):
     Tg, _, _ = guard.guard_thresholds(T, {kk: np.asarray(vv) for kk, vv in comp.items()})
     r = bsfa.prefill(x.q[None], x.k[None], x.v[None], block_q=Bq, block_k=Bk, mode="threshold",
                      thresholds=torch.from_numpy(Tg).to(dev), return_bitmap=True,
-                     return_lse=True, return_counts=True)
+                     return_lse=True, return_counts=True, mean_correction=mean_correction)
     torch.cuda.synchronize()
     assert bsfa.api.device_error() == 0
     bm = r["bitmap"].cpu().numpy().view(np.uint32)
     worst = _check_blocks(hc, blocks, Bq, Bk, sigma, L, bm, r["out"][0],
-                          r["lse"].reshape(Hq, L), "threshold", T=Tg.astype(np.float64))
+                          r["lse"].reshape(Hq, L), "threshold", T=Tg.astype(np.float64),
+                          mean_correction=mean_correction)
     kc, cand, diag = r["counts"].cpu().tolist()
     return worst, 1 - kc / cand
 
@@ -152,6 +153,13 @@ def _threshold_case(dev, name, k_index=0):
 def test_llama_32k_full_size(cuda_device):
     worst, skip = _threshold_case(cuda_device, "llama8b-L32768")
     assert 0.0 < skip < 1.0
+
+
+def test_llama_128k_k128_mean_correction_full_size(cuda_device):
+    """The bench's k = 128 slice at 128K with mean correction for the skipped
+    blocks (about 70% of the candidates get a stand-in)."""
+    worst, skip = _threshold_case(cuda_device, "llama8b-L131072", k_index=1, mean_correction=True)
+    assert 0.5 < skip < 1.0
 
 
 @pytest.mark.parametrize("k_index", [1, 2])

@@ -707,25 +707,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
       // Mean correction (Bq = Bk = 128: the candidates of query block I are
       // key blocks 0 .. I-1): kept bits of the candidates, one word per 32
       // blocks, in this warp's own shared-memory row.
-      const int ntt = nkt + (CORR ? (I + TILE - 1) / TILE : 0);
+      const int nct = CORR ? (I + TILE - 1) / TILE : 0;  // correction tiles after the keys
       uint32_t* my_kbits = kbits + (s * 4 + wq) * CORR_WORDS;
       uint32_t kbit_acc = 0;
 
-      for (int J = 0; J < ntt; ++J, ++tc) {
+      for (int J = 0; J < nkt; ++J, ++tc) {
         const int tb = tc & 1;
-        const bool corr_tile = CORR && J >= nkt;  // block means, not keys
-        // Correction tile: entry e stands for key block jb + e, which enters
-        // iff it is a candidate (jb + e < I) that this slot skipped.
-        uint32_t inc[4] = {0u, 0u, 0u, 0u};
-        if (corr_tile) {
-          const int jb = (J - nkt) * TILE;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int lim = I - jb - 32 * q;
-            const uint32_t cand = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
-            inc[q] = cand & ~my_kbits[(jb >> 5) + q];
-          }
-        }
         const uint32_t ph = (tc >> 1) & 1u;  // phase parity of the per-tile-parity barriers
         // Waits here are bounded.  In the gated kernel every thread joins the
         // per-tile vote barrier even after its own wait gave up, and the
@@ -750,12 +737,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
           tmem_wait_ld();
-          if (corr_tile) {
-#pragma unroll
-            for (int e = 0; e < 128; ++e)
-              if ((inc[e >> 5] >> (e & 31)) & 1u) rm0 = fmaxf(rm0, __uint_as_float(sr[e >> 5][e & 31]));
-            rm1 = rm0;
-          } else if (!diag_tile) {
+          if (!diag_tile) {
             rm0 = max3f(__uint_as_float(sr[0][0]), __uint_as_float(sr[0][1]),
                         __uint_as_float(sr[0][2]));
             rm1 = max3f(__uint_as_float(sr[2][0]), __uint_as_float(sr[2][1]),
@@ -850,13 +832,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
             // fence orders it before the barrier, so that the MMA warp may
             // overwrite S as soon as it reads a skip decision.
             tc_fence_before();
-            if (corr_tile) {
-              // Kept iff some block of the range was skipped (the same for
-              // every thread); the barrier only keeps the warpgroup together.
-              ok = bar_red_and(bar_id, 128, okl);
-              if (!ok) break;
-              keep[0][0] = (inc[0] | inc[1] | inc[2] | inc[3]) != 0u;
-            } else if (simple) {
+            if (simple) {
               // One 128x128 semantic block per tile: the hardware barrier
               // itself carries the vote (no shared-memory traffic, which
               // queues behind the MMAs' operand reads).  Lane 0 of each warp
@@ -884,7 +860,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
                 if (cls[1][k] == 1) keep[1][k] = (vq1 >> k) & 1u;
               }
             }
-            if (lambda_mode && !corr_tile) {
+            if (lambda_mode) {
               // Sub-blocks in ascending key order; a row's running max moves
               // only with the blocks it keeps, so the second key half is voted
               // on after the first half's decision.
@@ -925,9 +901,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
             const bool k0 = (myqs ? keep[1][0] : keep[0][0]);
             const bool k1 = (KS == 1) ? k0 : (myqs ? keep[1][1] : keep[0][1]);
             float rmk = -CUDART_INF_F;
-            // A stand-in's logit carries ln(Bk): one mean weighs Bk keys.
-            if (k0) rmk = fmaxf(rmk, corr_tile ? rm0 + p.corr_shift : rm0);
-            if (k1) rmk = fmaxf(rmk, corr_tile ? rm1 + p.corr_shift : rm1);
+            if (k0) rmk = fmaxf(rmk, rm0);
+            if (k1) rmk = fmaxf(rmk, rm1);
             const float m_new = fmaxf(m_used, rmk);
             const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
             float alpha = 1.f;
@@ -954,9 +929,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
             // columns have been read by then).
             const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * sc;
             const uint64_t sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
-            const float bias = corr_tile ? p.corr_shift * sc - mb : -mb;
             uint64_t lsum2 = f2_pack(0.f, 0.f);
-            const bool fast = !diag_tile && k0 && k1 && !corr_tile;
+            const bool fast = !diag_tile && k0 && k1;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               const bool kk = (hf == 0) ? k0 : k1;
@@ -982,14 +956,12 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                   const int cc = hf * 64 + 2 * e;
-                  const bool vis0 = corr_tile ? ((inc[cc >> 5] >> (cc & 31)) & 1u) != 0u
-                                              : kk && !(diag_tile && cc > row);
-                  const bool vis1 = corr_tile ? ((inc[(cc + 1) >> 5] >> ((cc + 1) & 31)) & 1u) != 0u
-                                              : kk && !(diag_tile && cc + 1 > row);
+                  const bool vis0 = kk && !(diag_tile && cc > row);
+                  const bool vis1 = kk && !(diag_tile && cc + 1 > row);
                   const float x0 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e) & 31]);
                   const float x1 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e + 1) & 31]);
-                  const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, bias)) : 0.f;
-                  const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, bias)) : 0.f;
+                  const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
+                  const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
                   lsum2 = f2_add(lsum2, f2_pack(p0, p1));
                   pk[e] = pack_x2<F16>(p0, p1);
                 }
@@ -1016,7 +988,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
               }
             }
           }
-          if (!corr_tile && lead_warp && my_i * p.Bq < len) {
+          if (lead_warp && my_i * p.Bq < len) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
               const int cl = (myqs ? cls[1][k] : cls[0][k]);
@@ -1041,6 +1013,102 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
         }
       }
       if (!ok) break;
+
+      if constexpr (CORR && GATING && !CALIB) {
+        // ---- mean-correction tiles: S = Q Kbar^T over the means of key
+        // blocks [jb, jb + 128).  Entry e enters iff key block jb + e is a
+        // candidate (jb + e < I) that this slot skipped; its logit carries
+        // ln(Bk) (corr_shift in raw score units), so one mean stands for the
+        // block's Bk keys.  The same hand-offs as a key tile: the vote
+        // barrier keeps the warpgroup together, the first warp publishes the
+        // decision (any entry), P goes over S and the MMA warp adds P Vbar.
+        for (int ci = 0; ci < nct; ++ci, ++tc) {
+          const int tb = tc & 1;
+          const int jb = ci * TILE;
+          uint32_t inc[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int lim = I - jb - 32 * q;
+            const uint32_t cand = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
+            inc[q] = cand & ~my_kbits[(jb >> 5) + q];
+          }
+          const bool any_in = (inc[0] | inc[1] | inc[2] | inc[3]) != 0u;
+          const bool okl = wait_bar(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL);
+          tc_fence_after();
+          float mx = -CUDART_INF_F;
+          if (okl && any_in) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t sq[32];
+              tmem_ld32(tS + q * 32, sq);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if ((inc[q] >> e) & 1u) mx = fmaxf(mx, __uint_as_float(sq[e]));
+            }
+          }
+          tc_fence_before();
+          if (!(ok = bar_red_and(bar_id, 128, okl))) break;
+          if (wq == 0) {  // all 32 lanes: same value, 32 arrivals
+            st_release_u32(&c->dec[s][tb],
+                           ((tc & DEC_STAMP_MASK) << DEC_BITS) | (any_in ? 1u : 0u));
+            mbar_arrive(&c->dec_full[s][tb]);
+          }
+          if (any_in) {
+            const float m_new = fmaxf(m_used, mx + p.corr_shift);
+            const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
+            float alpha = 1.f;
+            if (resc) {
+              alpha = ex2_approx((m_used - m_new) * sc);
+              m_used = m_new;
+              l *= alpha;
+            }
+            if (o_init && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+              for (int q = 0; q < D / 32; ++q) {
+                uint32_t orr[32];
+                tmem_ld32(tO + q * 32, orr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                tmem_st32(tO + q * 32, orr);
+              }
+            }
+            const float bias = p.corr_shift * sc - ((m_used == -CUDART_INF_F) ? 0.f : m_used * sc);
+            float lsum = 0.f;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+              // Re-read this half of S (64 columns) before P overwrites the
+              // first 32 columns of the S region with it.
+              uint32_t sh[2][32];
+              tmem_ld32(tS + hf * 64, sh[0]);
+              tmem_ld32(tS + hf * 64 + 32, sh[1]);
+              tmem_wait_ld();
+              const uint32_t m0 = inc[2 * hf], m1 = inc[2 * hf + 1];
+              uint32_t pk[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int c0 = 2 * e, c1 = 2 * e + 1;  // columns within this half
+                const uint32_t w0 = c0 < 32 ? m0 : m1, w1 = c1 < 32 ? m0 : m1;
+                const float x0 = __uint_as_float(sh[c0 >> 5][c0 & 31]);
+                const float x1 = __uint_as_float(sh[c1 >> 5][c1 & 31]);
+                const float p0 = ((w0 >> (c0 & 31)) & 1u) ? ex2_approx(fmaf(x0, sc, bias)) : 0.f;
+                const float p1 = ((w1 >> (c1 & 31)) & 1u) ? ex2_approx(fmaf(x1, sc, bias)) : 0.f;
+                lsum += p0 + p1;
+                pk[e] = pack_x2<F16>(p0, p1);
+              }
+              tmem_st32(tS + hf * 32, pk);
+            }
+            l += lsum;
+            tmem_wait_st();
+            o_init = true;
+          }
+          tc_fence_before();
+          mbar_arrive(&c->p_full[s][tb]);
+        }
+        if (!ok) break;
+      }
 
       if constexpr (!CALIB) {
         // ---- epilogue: O / l -> bf16, log-sum-exp, bitmap tail

@@ -167,6 +167,19 @@ def effective_flops(counts, Bq, Bk, d):
 
 
 # ----------------------------------------------------------------- our arm
+def aggregate_step(ms_step, step_flops, world, device=None):
+    """Whole-job figures of a weak-scaling run: every rank runs one replica of
+    the step, the step time is the maximum over ranks, and the value is the
+    FLOPs of all ranks over that time (TFLOP/s).  Returns (ms, value)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(ms_step)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    return ms_step, world * step_flops / (ms_step * 1e-3) / 1e12
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -222,15 +235,10 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     clocks = clk.summary()
     total_ms = t_start.elapsed_time(t_end)
-    ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    step_flops = sum(flops)
+    ms_step, value = aggregate_step(total_ms / args.steps, step_flops, world, dev)
     per_slice_ms = [statistics.mean(starts[s][i].elapsed_time(ends[s][i]) for s in range(args.steps))
                     for i in range(len(ks))]
-    step_flops = sum(flops)
-    value = world * step_flops / (ms_step * 1e-3) / 1e12
     launch_achieved = sum(flops) / (sum(per_slice_ms) * 1e-3) / 1e12
     slices_out = []
     for i, kk in enumerate(ks):

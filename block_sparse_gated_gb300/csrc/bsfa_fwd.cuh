@@ -389,13 +389,16 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
         // K for tile J + 1 (tile 0 before the loop proper), then V for tile J.
         if (J + 1 < ntt) {
           const uint32_t st = kc % KST;
+          // A paged tile's page comes from the block table: issue that load
+          // before the stage wait so that its latency hides behind it.
+          const int2 kc2 = (!CORR || J + 1 < nkt) ? kv_tile_coord<PAGED>(p, si, t.x, J + 1)
+                                                 : make_int2(0, 0);
           if (!(ok = wait_all(&c->k_empty[st], ((kc / KST) & 1) ^ 1, abort, p.err,
                               ERR_WAIT_K_EMPTY)))
             break;
           if (elect_one()) {
             mbar_arrive_expect_tx(&c->k_full[st], TB);
             if (!CORR || J + 1 < nkt) {
-              const int2 kc2 = kv_tile_coord<PAGED>(p, si, t.x, J + 1);
               for (int hf = 0; hf < NHALF; ++hf)
                 tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64, kc2.x, kvh,
                             kc2.y);
@@ -412,11 +415,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
         if constexpr (!CALIB && !GATING) {
           {
             const uint32_t st = vc % VST;
+            const int2 vc2 = kv_tile_coord<PAGED>(p, si, t.x, J);  // before the wait
             if (!(ok = wait_all(&c->v_empty[st], ((vc / VST) & 1) ^ 1, abort, p.err,
                                 ERR_WAIT_V_EMPTY)))
               break;
             if (elect_one()) {
-              const int2 vc2 = kv_tile_coord<PAGED>(p, si, t.x, J);
               mbar_arrive_expect_tx(&c->v_full[st], TB);
               for (int hf = 0; hf < NHALF; ++hf)
                 tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64, vc2.x, kvh,
@@ -461,6 +464,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
         // decision is read: V of every tile is issued as early as a stage
         // is free, like the gate-compiled-out producer does.
         bool need = VALL, issued = false;
+        // The tile's V coordinates (a block-table load when paged) are read
+        // before the decision waits, off the path from a keep to its copy.
+        const int2 vc2 = (!CORR || J < nkt) ? kv_tile_coord<PAGED>(p, si, t.x, J) : make_int2(0, 0);
         for (int s = 0; s < NQ && ok; ++s) {
           if constexpr (!VALL) {
             if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
@@ -477,7 +483,6 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
           if (elect_one()) {
             mbar_arrive_expect_tx(&c->v_full[st], TB);
             if (!CORR || J < nkt) {
-              const int2 vc2 = kv_tile_coord<PAGED>(p, si, t.x, J);
               for (int hf = 0; hf < NHALF; ++hf)
                 tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64, vc2.x, kvh,
                             vc2.y);

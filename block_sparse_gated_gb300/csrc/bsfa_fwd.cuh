@@ -738,7 +738,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
         // ---- pass 1: row maxima of the two 64-key halves of S
         float rm0 = -CUDART_INF_F, rm1 = -CUDART_INF_F;
         uint32_t sr[4][32];
-        if (okl) {
+        // Unconditional, even for a thread whose wait gave up (it then reads
+        // stale S from its own TMEM columns and the vote barrier stops the
+        // warpgroup): a per-thread guard around the .sync.aligned loads cost
+        // the gated kernel about 2% of its tile period.
+        {
 #pragma unroll
           for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
           tmem_wait_ld();

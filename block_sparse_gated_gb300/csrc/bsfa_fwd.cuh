@@ -743,23 +743,17 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
         // warpgroup): a per-thread guard around the .sync.aligned loads cost
         // the gated kernel about 2% of its tile period.
         {
+          // The reducing TMEM load returns each 32-column quarter's maximum
+          // along with the values, so a tile below the diagonal needs no
+          // max instructions at all; the diagonal tile masks and reduces the
+          // values itself.
+          float qm[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
+          for (int q = 0; q < 4; ++q) tmem_ld32_max(tS + q * 32, sr[q], qm[q]);
           tmem_wait_ld();
           if (!diag_tile) {
-            rm0 = max3f(__uint_as_float(sr[0][0]), __uint_as_float(sr[0][1]),
-                        __uint_as_float(sr[0][2]));
-            rm1 = max3f(__uint_as_float(sr[2][0]), __uint_as_float(sr[2][1]),
-                        __uint_as_float(sr[2][2]));
-#pragma unroll
-            for (int e = 3; e < 63; e += 2) {
-              rm0 = max3f(rm0, __uint_as_float(sr[e >> 5][e & 31]),
-                          __uint_as_float(sr[(e + 1) >> 5][(e + 1) & 31]));
-              rm1 = max3f(rm1, __uint_as_float(sr[2 + (e >> 5)][e & 31]),
-                          __uint_as_float(sr[2 + ((e + 1) >> 5)][(e + 1) & 31]));
-            }
-            rm0 = fmaxf(rm0, __uint_as_float(sr[1][31]));
-            rm1 = fmaxf(rm1, __uint_as_float(sr[3][31]));
+            rm0 = fmaxf(qm[0], qm[1]);
+            rm1 = fmaxf(qm[2], qm[3]);
           } else {
 #pragma unroll
             for (int e = 0; e < 128; ++e) {

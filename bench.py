@@ -51,6 +51,28 @@ def _recorded_traffic(workload):
         return None
 
 
+def _recorded_ncu(workload="llama8b-L32768"):
+    """Tensor-pipe utilisation and DRAM GB/s from the committed full ncu
+    capture of the prefill kernel, or None when the kernel sources changed
+    since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"bsfa_fwd_kernel_full_{workload}.json")
+    try:
+        rec = json.load(open(path))
+        h = hashlib.sha256()
+        for f in rec["sources"]:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return {"workload": rec["workload"], "kernel": rec["kernel"],
+                "tensor_pipe_active_pct": rec["tensor_pipe_active_pct_of_elapsed"],
+                "dram_gbps": rec["dram_gbps"],
+                "dram_pct_of_peak": rec["dram_throughput_pct_of_peak"],
+                "source": os.path.relpath(path, ROOT)}
+    except Exception:
+        return None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -270,7 +292,8 @@ def run_ours(args, rank, world, local_rank):
                      "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
                      "frac_of_burst": round(launch_achieved / peak_burst, 4),
                      "traffic": _recorded_traffic(args.workload),
-                     "traffic_unit": "bytes per launch (ncu dram read + write)"},
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
+                     "ncu": _recorded_ncu()},
         "clocks": clocks,
         "gpu_launches": 2 * len(ks) * args.steps,
         "calibrate": {"ms": round(W["cal_ms"], 3), "samples": cfg["n_cal"],

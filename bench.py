@@ -34,17 +34,27 @@ METRIC = ("prefill attention ms/layer & effective TFLOPS (frac of bf16 peak) at 
 UNIT = "TFLOP/s (effective)"
 
 
+def code_digest(paths):
+    """sha256 of the given sources with C/C++ comments and all whitespace
+    removed: it changes when the code changes, not when a comment does."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for p in paths:
+        text = open(os.path.join(ROOT, p)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(re.sub(r"\s+", "", text).encode())
+    return h.hexdigest()
+
+
 def _recorded_traffic(workload):
     """Mean DRAM bytes per launch of the prefill kernel from the committed ncu
-    record, or None when the kernel sources changed since it was taken."""
-    import hashlib
+    record, or None when the kernel code changed since it was taken."""
     path = os.path.join(ROOT, "profiles", f"bsfa_fwd_kernel_dram_{workload}.json")
     try:
         rec = json.load(open(path))
-        h = hashlib.sha256()
-        for f in rec["sources"]:
-            h.update(open(os.path.join(ROOT, f), "rb").read())
-        if h.hexdigest() != rec["sources_sha256"]:
+        if code_digest(rec["sources"]) != rec["code_sha256"]:
             return None
         return float(rec["mean_bytes_per_launch"])
     except Exception:
@@ -53,16 +63,12 @@ def _recorded_traffic(workload):
 
 def _recorded_ncu(workload="llama8b-L32768"):
     """Tensor-pipe utilisation and DRAM GB/s from the committed full ncu
-    capture of the prefill kernel, or None when the kernel sources changed
-    since it was taken."""
-    import hashlib
+    capture of the prefill kernel, or None when the kernel code changed since
+    it was taken."""
     path = os.path.join(ROOT, "profiles", f"bsfa_fwd_kernel_full_{workload}.json")
     try:
         rec = json.load(open(path))
-        h = hashlib.sha256()
-        for f in rec["sources"]:
-            h.update(open(os.path.join(ROOT, f), "rb").read())
-        if h.hexdigest() != rec["sources_sha256"]:
+        if code_digest(rec["sources"]) != rec["code_sha256"]:
             return None
         return {"workload": rec["workload"], "kernel": rec["kernel"],
                 "tensor_pipe_active_pct": rec["tensor_pipe_active_pct_of_elapsed"],

@@ -22,6 +22,12 @@
 //
 // TMEM columns: S_s at [128 s, 128 s + 128) (P_s overwrites its first 64
 // columns as packed bf16 pairs), O_s at [128 NQ + D s, 128 NQ + D (s+1)).
+//
+// Compiled-in options (template parameters, so that no option costs the
+// others a branch): the gate or none, the calibration variant (Q.K^T and
+// block maxima only), fp16 or bf16 elements, V for every tile (an A/B of the
+// gated V load), K/V read from page pools through a block table, and
+// mean-correction tiles after a unit's key tiles.
 #pragma once
 #include <cuda_bf16.h>
 #include <math_constants.h>

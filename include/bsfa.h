@@ -32,6 +32,10 @@
  *     expected in a correct run) sets a device error word; it is reported by
  *     bsfa_device_error.
  *   - No C++ exception crosses this boundary.
+ *   - Size limits (BSFA_ERR_UNSUPPORTED beyond them): at most 4096 sequences
+ *     per call; at most 16384 query tiles of 128 rows per sequence (2M tokens);
+ *     for calibration, at most 16 budgets per call and 8192 key blocks per
+ *     sample.
  *
  * Block geometry (all positions local to a sequence):
  *   query block i covers rows [i*Bq, min((i+1)*Bq, L)); key block j covers

@@ -162,6 +162,31 @@ def test_mean_correction_parameters_are_validated_on_the_host(libpath):
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # contiguous K/V only
 
 
+def test_size_limits_are_rejected_on_the_host(libpath):
+    """The documented limits: 4096 sequences per call, 16384 query tiles of
+    128 rows per sequence; calibration: 16 budgets, 8192 key blocks."""
+    import ctypes
+    from block_sparse_gated_gb300 import _native
+    L = _native.lib()
+    p = _native.FwdParams()
+    p.batch, p.num_heads_q, p.num_heads_kv, p.head_dim = 1, 2, 2, 128
+    p.block_q = p.block_k = 128
+    p.mode = 2
+    p.seqlen = 16384 * 128 + 1
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # one tile too many
+    p.seqlen, p.batch = 1024, 4097
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # too many sequences
+    assert L.bsfa_prefill_workspace_size(ctypes.byref(p)) == 0
+    dummy = (ctypes.c_void_p * 1)(1 << 20)
+    st = (ctypes.c_int64 * 2)(1024 * 128, 128)
+    out = ctypes.c_void_p(1 << 20)
+    ks = (ctypes.c_int * 17)(*range(1, 18))
+    assert L.bsfa_calibrate(dummy, dummy, 1, 2, 2, 1024, 128, 0, st, st, 128, 128, 0.0, ks, 17,
+                            out, out, 1 << 30, None) == 2  # 17 budgets
+    assert L.bsfa_calibrate(dummy, dummy, 1, 2, 2, 8193 * 128, 128, 0, st, st, 128, 128, 0.0,
+                            ks, 1, out, out, 1 << 30, None) == 2  # 8193 key blocks
+
+
 def test_mixed_element_types_are_rejected_before_the_library():
     import torch
     from block_sparse_gated_gb300 import api

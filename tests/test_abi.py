@@ -200,3 +200,27 @@ def test_mixed_element_types_are_rejected_before_the_library():
         api._params(q.float(), q.float(), q.float(), q.float(), layout=None, cu_seqlens=None,
                     max_seqlen=None, block_q=128, block_k=128, softmax_scale=None, mode="none",
                     thresholds=None, log_lambda=None)
+
+
+def test_binding_checks_paged_arguments():
+    """The Python binding's own checks of page pools and block tables (before
+    the library sees the call)."""
+    import torch
+    from block_sparse_gated_gb300 import api
+    q = torch.zeros(1, 4, 300, 128, dtype=torch.bfloat16)
+    pool = torch.zeros(3, 256, 2, 128, dtype=torch.bfloat16)  # [pages, page_size, Hkv, d]
+    table = torch.zeros(1, 2, dtype=torch.int32)
+    kw = dict(layout=None, cu_seqlens=None, max_seqlen=None, block_q=128, block_k=128,
+              softmax_scale=None, mode="none", thresholds=None, log_lambda=None)
+    p = api._params(q, pool, pool, q, block_table=table, **kw)
+    assert (p.page_size, p.num_pages, p.block_table_stride) == (256, 3, 2)
+    assert tuple(p.k_stride) == (256 * 2 * 128, 128, 2 * 128)
+    p = api._params(q, pool.permute(0, 2, 1, 3).contiguous(), pool.permute(0, 2, 1, 3).contiguous(),
+                    q, block_table=table, kv_layout="phtd", **kw)
+    assert (p.page_size, tuple(p.k_stride)) == (256, (2 * 256 * 128, 256 * 128, 128))
+    with pytest.raises(ValueError):
+        api._params(q, pool, pool, q, block_table=table.long(), **kw)  # int32 table only
+    with pytest.raises(ValueError):
+        api._params(q, pool, pool[:, :128], q, block_table=table, **kw)  # pools disagree
+    p = api._params(q, q[:, :2], q[:, :2], q, mean_correction=True, **kw)
+    assert p.flags == 2

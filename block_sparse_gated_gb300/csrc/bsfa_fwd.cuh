@@ -119,6 +119,7 @@ struct Ctrl {
   // slot; calibration maxima of a slot's four warps in (128 arrivals); the
   // decision word published by the slot's first warp (32 arrivals).
   uint64_t p_full[NQ][2];
+  uint64_t ph_full[NQ][2];  // first half of P (keys 0-63) written
   uint64_t red_full[NQ][2];
   uint64_t dec_full[NQ][2];
   uint64_t drain;
@@ -281,6 +282,18 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
     umma_ts(d_tmem, p_tmem + kk * 8, dv + ((kk * 2048) >> 4), idesc, (kk > 0 || acc) ? 1u : 0u);
 }
 
+// One half of O (+)= P V: K-steps [4 half, 4 half + 4), i.e. keys
+// [64 half, 64 half + 64), whose P lives in TMEM columns [32 half, 32 half + 32).
+template <int D, int NQ>
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv,
+                                              uint32_t idesc, uint32_t acc, int half) {
+#pragma unroll
+  for (int k = 0; k < TILE / 32; ++k) {
+    const int kk = half * (TILE / 32) + k;
+    umma_ts(d_tmem, p_tmem + kk * 8, dv + ((kk * 2048) >> 4), idesc, (kk > 0 || acc) ? 1u : 0u);
+  }
+}
+
 // VALL (gated only): load V for every visible tile, kept or not.
 // PAGED: K and V come from page pools through the block table.
 // CORR (gated, Bq = Bk = 128): mean correction.  After a unit's key tiles,
@@ -321,6 +334,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
       for (int b = 0; b < 2; ++b) {
         mbar_init(&c->p_full[s][b], 128);
         mbar_init(&c->red_full[s][b], 128);
+        mbar_init(&c->ph_full[s][b], 128);
         mbar_init(&c->dec_full[s][b], 32);
       }
     }
@@ -614,15 +628,37 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
           // is published only after the vote barrier of tile tc - 1, which
           // each thread reaches after its arrival for tile tc - 2), so a
           // later wait on it never falls two phases behind.
-          if ((CALIB || !GATING || do_pv) && !p_ok) {
-            if (!(ok = wait_all(&c->p_full[s][tb], ppar, abort, p.err, ERR_WAIT_P_FULL))) break;
+          if (CALIB) {
+            if (!p_ok && !(ok = wait_all(&c->p_full[s][tb], ppar, abort, p.err, ERR_WAIT_P_FULL)))
+              break;
+            tc_fence_after();
+          } else if (do_pv) {
+            // P.V for this tile first: it does not need the next K tile.
+            const uint32_t d_o = tmem + NQ * 128 + s * D, d_p = tmem + s * 128;
+            const uint64_t dv_st = dV + ((vst * TB) >> 4);
+            if (GATING && !p_ok) {
+              // The softmax hands P off in two halves: start on keys 0-63
+              // while it still computes keys 64-127.
+              if (!(ok = wait_all(&c->ph_full[s][tb], ppar, abort, p.err, ERR_WAIT_P_FULL)))
+                break;
+              tc_fence_after();
+              if (elect_one()) issue_pv_half<D, NQ>(d_o, d_p, dv_st, IDESC_PV, acc, 0);
+              __syncwarp();
+              if (!(ok = wait_all(&c->p_full[s][tb], ppar, abort, p.err, ERR_WAIT_P_FULL))) break;
+              tc_fence_after();
+              if (elect_one()) issue_pv_half<D, NQ>(d_o, d_p, dv_st, IDESC_PV, 1u, 1);
+              __syncwarp();
+            } else {
+              if (!GATING && !p_ok &&
+                  !(ok = wait_all(&c->p_full[s][tb], ppar, abort, p.err, ERR_WAIT_P_FULL)))
+                break;
+              tc_fence_after();
+              if (elect_one()) issue_pv<D, NQ>(d_o, d_p, dv_st, IDESC_PV, acc);
+              __syncwarp();
+            }
+          } else {
+            tc_fence_after();
           }
-          tc_fence_after();
-          // P.V for this tile first: it does not need the next K tile.
-          if (do_pv && elect_one())
-            issue_pv<D, NQ>(tmem + NQ * 128 + s * D, tmem + s * 128, dV + ((vst * TB) >> 4),
-                            IDESC_PV, acc);
-          __syncwarp();
           if (do_qk && s == 0 && !k_ok) {
             if (!(ok = wait_all(&c->k_full[kst], (kc / KST) & 1, abort, p.err, ERR_WAIT_K_FULL)))
               break;
@@ -976,6 +1012,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
                 }
               }
               tmem_st32(tS + hf * 32, pk);
+              if (GATING && hf == 0) {  // hand off the first half of P
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&c->ph_full[s][tb]);
+              }
             }
             float ls0, ls1;
             f2_unpack(lsum2, ls0, ls1);
@@ -983,6 +1024,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
             tmem_wait_st();
             o_init = true;
           }
+          if (GATING && decbits == 0u) mbar_arrive(&c->ph_full[s][tb]);  // one phase per tile
           tc_fence_before();
           mbar_arrive(&c->p_full[s][tb]);
 
@@ -1108,11 +1150,17 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
                 pk[e] = pack_x2<F16>(p0, p1);
               }
               tmem_st32(tS + hf * 32, pk);
+              if (hf == 0) {
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&c->ph_full[s][tb]);
+              }
             }
             l += lsum;
             tmem_wait_st();
             o_init = true;
           }
+          if (!any_in) mbar_arrive(&c->ph_full[s][tb]);
           tc_fence_before();
           mbar_arrive(&c->p_full[s][tb]);
         }

@@ -38,8 +38,7 @@ Sources (page title, section):
   (one row that wants the block vetoes the skip); a skipped block leaves the
   running max untouched; the running max used for the vote is exact.
 
-Readings taken where the pages are silent or ambiguous (each is listed in
-the design doc with its reason):
+Readings taken where the pages are silent or ambiguous:
 
 * ">=" (not ">") in the threshold test.
 * Candidate ("off-diagonal") key block j for query block i: every key of j

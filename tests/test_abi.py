@@ -132,6 +132,8 @@ def test_paged_parameters_are_validated_on_the_host(libpath):
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2
     p.k_stride[0] = 256 * 2 * 128
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 5  # all fine up to the missing workspace
+    p.flags = _native.FLAG_V_ALWAYS
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # no paged V-always kernels
 
 
 def test_mean_correction_parameters_are_validated_on_the_host(libpath):

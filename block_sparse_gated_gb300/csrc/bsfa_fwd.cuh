@@ -627,7 +627,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
           // followed either the P of tile tc - 1, or a skip decision, which
           // is published only after the vote barrier of tile tc - 1, which
           // each thread reaches after its arrival for tile tc - 2), so a
-          // later wait on it never falls two phases behind.
+          // later wait on it never falls two phases behind.  The barrier of
+          // P's first half (ph_full) gets one arrival per thread per tile as
+          // well, before that thread's P arrival, so the same holds for it.
           if (CALIB) {
             if (!p_ok && !(ok = wait_all(&c->p_full[s][tb], ppar, abort, p.err, ERR_WAIT_P_FULL)))
               break;

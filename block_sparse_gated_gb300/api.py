@@ -33,9 +33,35 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _stream(stream, device=None):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _on_device(device, **tensors):
+    """Every tensor the library dereferences must live on ``device`` (a CUDA
+    device): a host pointer reaching a kernel is a fault, not an error code."""
+    if device.type != "cuda":
+        raise ValueError("q must be a CUDA tensor")
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _user_workspace(workspace, need: int, device):
+    """The caller's workspace if it is a contiguous buffer of at least ``need``
+    bytes on ``device``, else a fresh byte buffer."""
+    if workspace is not None:
+        if not workspace.is_contiguous():
+            raise ValueError("the workspace must be contiguous")
+        _on_device(device, workspace=workspace)
+        if _nbytes(workspace) >= need:
+            return workspace
+    return torch.empty(max(need, 256), dtype=torch.uint8, device=device)
 
 
 _DTYPES = {torch.bfloat16: _native.DTYPE_BF16, torch.float16: _native.DTYPE_F16}
@@ -112,6 +138,25 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
     if not (q.dtype == k.dtype == v.dtype == o.dtype):
         raise TypeError("Q, K, V and O must share one element type")
     d = q.shape[-1]
+    if not (k.shape[-1] == v.shape[-1] == o.shape[-1] == d):
+        raise ValueError("Q/K/V/O head dimensions disagree")
+    # The library takes the batch size from q: o (and k, v unless they are
+    # page pools) must have the same rank and batch extent.
+    same_batch = [o] if paged else [k, v, o]
+    if any(t.dim() != q.dim() or (q.dim() == 4 and t.shape[0] != q.shape[0])
+           for t in same_batch):
+        raise ValueError("Q/K/V/O batch shapes disagree")
+    if varlen:
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or \
+                not cu_seqlens.is_contiguous() or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be a contiguous int32 [batch + 1] tensor")
+        if max_seqlen is None:
+            raise ValueError("varlen calls need max_seqlen")
+    if paged:
+        nb = cu_seqlens.numel() - 1 if varlen else (1 if q.dim() == 3 else q.shape[0])
+        longest = int(max_seqlen) if varlen else Lq
+        if block_table.shape[0] < nb or block_table.shape[1] * page < longest:
+            raise ValueError("block_table has fewer rows than sequences or too few pages per row")
     p = _native.FwdParams()
     p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
     p.q_stride[:], p.k_stride[:], p.v_stride[:], p.o_stride[:] = qs, ks, vs, os_
@@ -128,7 +173,8 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
     p.softmax_scale = float(softmax_scale) if softmax_scale else 0.0
     p.mode = _MODES[mode] if isinstance(mode, str) else int(mode)
     if thresholds is not None:
-        if thresholds.dtype != torch.float32 or thresholds.dim() != 2 or not thresholds.is_contiguous():
+        if thresholds.dtype != torch.float32 or thresholds.dim() != 2 or \
+                not thresholds.is_contiguous() or thresholds.shape[0] != Hq:
             raise ValueError("thresholds must be a contiguous float32 [Hq, nT] tensor")
         p.thresholds, p.thresholds_nq = thresholds.data_ptr(), thresholds.shape[1]
     else:
@@ -178,13 +224,15 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
     key count (threshold and lambda modes, 128 x 128 blocks, contiguous K/V)."""
     if out is None:
         out = torch.empty_like(q)
+    dev = q.device
+    _on_device(dev, k=k, v=v, out=out, thresholds=thresholds, cu_seqlens=cu_seqlens,
+               block_table=block_table)
     p = _params(q, k, v, out, layout=layout, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
                 block_q=block_q, block_k=block_k, softmax_scale=softmax_scale, mode=mode,
                 thresholds=thresholds, log_lambda=log_lambda, v_always=v_always,
                 block_table=block_table, kv_layout=kv_layout, mean_correction=mean_correction)
     L = _native.lib()
     res = {"out": out}
-    dev = q.device
     if return_bitmap:
         if cu_seqlens is not None:
             cu = cu_seqlens.cpu().tolist()
@@ -207,11 +255,9 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
         cnt = torch.empty(3, dtype=torch.int64, device=dev)
         p.block_counts = cnt.data_ptr()
         res["counts"] = cnt
-    need = L.bsfa_prefill_workspace_size(ctypes.byref(p))
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
-    _check(L.bsfa_prefill_fwd(ctypes.byref(p), _stream(stream)), "bsfa_prefill_fwd")
+    workspace = _user_workspace(workspace, L.bsfa_prefill_workspace_size(ctypes.byref(p)), dev)
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), _nbytes(workspace)
+    _check(L.bsfa_prefill_fwd(ctypes.byref(p), _stream(stream, dev)), "bsfa_prefill_fwd")
     return res
 
 
@@ -243,13 +289,21 @@ def calibrate(q_samples, k_samples, ks, *, block_q=128, block_k=128, softmax_sca
         if t.dtype != q0.dtype or t.stride(-1) != 1 or t.shape[1] != Ltok or t.shape[2] != d:
             raise ValueError("samples must be [H, L, d] of one type with d contiguous and equal L")
     dcode = _dtype_code(q0)
+    dev = q0.device
+    _on_device(dev, **{f"sample {i}": t for i, t in enumerate(list(q_samples) + list(k_samples))})
+    for t in k_samples:
+        if t.shape[0] != Hkv:
+            raise ValueError("all k samples must have the same number of heads")
     nq = (Ltok + block_q - 1) // block_q
     if out is None:
-        out = torch.empty((len(ks), Hq, nq), dtype=torch.float32, device=q0.device)
+        out = torch.empty((len(ks), Hq, nq), dtype=torch.float32, device=dev)
+    elif out.dtype != torch.float32 or not out.is_contiguous() or \
+            tuple(out.shape) != (len(ks), Hq, nq):
+        raise ValueError(f"out must be a contiguous float32 [{len(ks)}, {Hq}, {nq}] tensor")
+    _on_device(dev, out=out)
     L = _native.lib()
-    need = L.bsfa_calibrate_workspace_size(Hq, Ltok, block_q, block_k)
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q0.device)
+    workspace = _user_workspace(workspace, L.bsfa_calibrate_workspace_size(Hq, Ltok, block_q,
+                                                                           block_k), dev)
     qp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in q_samples])
     kp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in k_samples])
     qst = (ctypes.c_int64 * 2)(q0.stride(0), q0.stride(1))
@@ -264,8 +318,8 @@ def calibrate(q_samples, k_samples, ks, *, block_q=128, block_k=128, softmax_sca
     scale = float(softmax_scale) if softmax_scale else 0.0
     _check(L.bsfa_calibrate(qp, kp, n, Hq, Hkv, Ltok, d, dcode, qst, kst, block_q, block_k, scale,
                             karr, len(ks), ctypes.c_void_p(out.data_ptr()),
-                            ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                            _stream(stream)), "bsfa_calibrate")
+                            ctypes.c_void_p(workspace.data_ptr()), _nbytes(workspace),
+                            _stream(stream, dev)), "bsfa_calibrate")
     return out
 
 

@@ -226,3 +226,64 @@ def test_binding_checks_paged_arguments():
         api._params(q, pool, pool[:, :128], q, block_table=table, **kw)  # pools disagree
     p = api._params(q, q[:, :2], q[:, :2], q, mean_correction=True, **kw)
     assert p.flags == 2
+
+
+def test_binding_rejects_host_tensors_before_the_library():
+    """Host tensors never reach a kernel: the binding refuses them."""
+    import torch
+    from block_sparse_gated_gb300 import api
+    q = torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.prefill(q, q, q, mode="none")
+    with pytest.raises(ValueError, match="CUDA"):
+        api.calibrate([q[0]], [q[0]], [1])
+    with pytest.raises(ValueError, match="expected cuda:0"):
+        api._on_device(torch.device("cuda", 0), thresholds=torch.zeros(2, 1))
+
+
+def test_binding_checks_shapes_the_library_cannot_see():
+    """Extents that the C ABI takes from q alone (batch, head dimension, the
+    threshold table's rows, the block table's rows and columns) are checked
+    against every other tensor before the call."""
+    import torch
+    from block_sparse_gated_gb300 import api
+    bf = torch.bfloat16
+    q = torch.zeros(2, 4, 300, 128, dtype=bf)
+    kv = torch.zeros(2, 2, 300, 128, dtype=bf)
+    kw = dict(layout=None, cu_seqlens=None, max_seqlen=None, block_q=128, block_k=128,
+              softmax_scale=None, mode="none", thresholds=None, log_lambda=None)
+    p = api._params(q, kv, kv, q, **kw)
+    assert (p.batch, p.num_heads_q, p.num_heads_kv, p.seqlen, p.head_dim) == (2, 4, 2, 300, 128)
+    with pytest.raises(ValueError, match="head dimensions"):
+        api._params(q, kv[..., :64], kv[..., :64], q, **kw)
+    with pytest.raises(ValueError, match="batch"):
+        api._params(q, kv[:1], kv[:1], q, **kw)
+    with pytest.raises(ValueError, match="batch"):
+        api._params(q, kv, kv, q[:1], **kw)
+    with pytest.raises(ValueError, match="batch"):
+        api._params(q[0], kv, kv, q[0], **kw)  # one sequence with batched K/V
+    thr = dict(kw, mode="threshold")
+    api._params(q, kv, kv, q, **dict(thr, thresholds=torch.zeros(4, 3)))
+    with pytest.raises(ValueError, match="thresholds"):
+        api._params(q, kv, kv, q, **dict(thr, thresholds=torch.zeros(2, 3)))  # rows != Hq
+    # varlen: int32 offsets and a max_seqlen
+    qv, kvv = torch.zeros(4, 300, 128, dtype=bf), torch.zeros(2, 300, 128, dtype=bf)
+    cu = torch.tensor([0, 100, 300], dtype=torch.int32)
+    p = api._params(qv, kvv, kvv, qv, **dict(kw, cu_seqlens=cu, max_seqlen=200))
+    assert (p.batch, p.max_seqlen) == (2, 200)
+    with pytest.raises(ValueError, match="cu_seqlens"):
+        api._params(qv, kvv, kvv, qv, **dict(kw, cu_seqlens=cu.long(), max_seqlen=200))
+    with pytest.raises(ValueError, match="max_seqlen"):
+        api._params(qv, kvv, kvv, qv, **dict(kw, cu_seqlens=cu))
+    # paged: one table row per sequence, enough pages for the longest one
+    pool = torch.zeros(6, 128, 2, 128, dtype=bf)
+    api._params(q, pool, pool, q, block_table=torch.zeros(2, 3, dtype=torch.int32), **kw)
+    with pytest.raises(ValueError, match="block_table"):
+        api._params(q, pool, pool, q, block_table=torch.zeros(1, 3, dtype=torch.int32), **kw)
+    with pytest.raises(ValueError, match="block_table"):
+        api._params(q, pool, pool, q, block_table=torch.zeros(2, 2, dtype=torch.int32), **kw)
+    api._params(qv, pool, pool, qv, block_table=torch.zeros(2, 2, dtype=torch.int32),
+                **dict(kw, cu_seqlens=cu, max_seqlen=200))
+    with pytest.raises(ValueError, match="block_table"):
+        api._params(qv, pool, pool, qv, block_table=torch.zeros(2, 1, dtype=torch.int32),
+                    **dict(kw, cu_seqlens=cu, max_seqlen=200))

@@ -1,0 +1,119 @@
+"""Planted mistakes in the fp64 oracle, for checking that its pins catch them.
+
+Each entry of ``MUTANTS`` is (name, original text, replacement) for one
+plausible slip in ``oracle/bsfa_oracle.py``: a flipped comparison, a dropped
+term, a wrong index, a swapped visiting order.  The original text must occur
+exactly once in the oracle's source, so a mutant that no longer applies is an
+error rather than a silent pass.
+
+Loaded as a pytest plugin (``-p tests.oracle_mutants``) with the environment
+variable ``BSFA_ORACLE_MUTANT`` naming one entry, it builds that mutant of the
+oracle module on the CPU and installs it in place of ``oracle.bsfa_oracle``
+for the test session; the oracle's file is not touched.  Without the variable
+it does nothing.
+"""
+import os
+import sys
+import types
+
+ENV = "BSFA_ORACLE_MUTANT"
+
+MUTANTS = [
+    # block geometry and the score matrix
+    ("partial_blocks_as_candidates", "if (j + 1) * Bk <= first_row:",
+     "if j * Bk <= first_row:"),
+    ("last_row_window_shrinks", "if first_key <= last_row:", "if first_key < last_row:"),
+    ("causal_mask_excludes_self", "s = np.where(cols[None, :] <= rows[:, None], s, NEG_INF)",
+     "s = np.where(cols[None, :] < rows[:, None], s, NEG_INF)"),
+    ("no_softmax_scale", "s = sigma * (q_h[r0:r1] @ k_h[:r1].T)", "s = q_h[r0:r1] @ k_h[:r1].T"),
+    ("tile_mean_not_max", "return float(np.max(s[:, j * Bk:(j + 1) * Bk]))",
+     "return float(np.mean(s[:, j * Bk:(j + 1) * Bk]))"),
+    ("tile_max_first_row_only", "return float(np.max(s[:, j * Bk:(j + 1) * Bk]))",
+     "return float(np.max(s[0, j * Bk:(j + 1) * Bk]))"),
+    # threshold gate
+    ("gt_instead_of_ge", "keep[j] = tile_max(s, j, Bk) >= T_hi",
+     "keep[j] = tile_max(s, j, Bk) > T_hi"),
+    ("diagonal_gated",
+     "            keep[j] = True\n        else:\n            keep[j] = tile_max(s, j, Bk) >= T_hi",
+     "            keep[j] = tile_max(s, j, Bk) >= T_hi\n        else:\n"
+     "            keep[j] = tile_max(s, j, Bk) >= T_hi"),
+    ("gqa_modulo", "return h // (Hq // Hkv)", "return h % Hkv"),
+    ("threshold_by_kv_head",
+     "T_hi = float(thresholds[h][threshold_index(i, len(thresholds[h]))])",
+     "T_hi = float(thresholds[kh][threshold_index(i, len(thresholds[kh]))])"),
+    ("threshold_index_wraps", "return min(i, nT - 1)", "return i % nT"),
+    # renormalised attention
+    ("lse_drops_max", "lse = (M + np.log(Z))[:, 0]", "lse = np.log(Z)[:, 0]"),
+    ("skipped_keys_in_denominator", "Z = np.sum(e, axis=1, keepdims=True)",
+     "Z = np.sum(np.exp(s - M), axis=1, keepdims=True)"),
+    ("output_not_normalised", "out = (e @ vals) / Z", "out = e @ vals"),
+    # calibration
+    ("kth_plus_one", "return float(sorted(values, reverse=True)[k - 1])",
+     "return float(sorted(values, reverse=True)[min(k, len(values) - 1)])"),
+    ("kth_smallest", "return float(sorted(values, reverse=True)[k - 1])",
+     "return float(sorted(values)[k - 1])"),
+    ("short_history_not_minus_inf",
+     "    if len(values) < k:\n        return NEG_INF\n"
+     "    return float(sorted(values, reverse=True)[k - 1])",
+     "    if not values:\n        return NEG_INF\n"
+     "    return float(sorted(values, reverse=True)[min(k, len(values)) - 1])"),
+    ("calibration_sums_samples", "T[:, h, i] = acc / N", "T[:, h, i] = acc"),
+    # lambda gate
+    ("lambda_running_max_frozen", "            m = np.maximum(m, rowmax)",
+     "            m = np.where(np.isinf(m), rowmax, m)"),
+    ("lambda_one_row_skips", "kept = not bool(np.all(stat < log_lambda))",
+     "kept = not bool(np.any(stat < log_lambda))"),
+    ("lambda_skip_at_bound", "kept = not bool(np.all(stat < log_lambda))",
+     "kept = not bool(np.all(stat <= log_lambda))"),
+    ("lambda_log2_bound", "kept = not bool(np.all(stat < log_lambda))",
+     "kept = not bool(np.all(stat < log_lambda / math.log(2.0)))"),
+    ("lambda_tile_max_statistic", "rowmax = np.max(s[:, j * Bk:(j + 1) * Bk], axis=1)",
+     "rowmax = np.full(s.shape[0], np.max(s[:, j * Bk:(j + 1) * Bk]))"),
+    ("lambda_descending", "return cands + diags", "return cands[::-1] + diags"),
+    ("lambda_diagonal_first", "return cands + diags", "return diags + cands"),
+    # mean correction
+    ("stand_in_without_count", "logits[:, n] = sigma * (q_rows @ kbar) + math.log(c1 - c0)",
+     "logits[:, n] = sigma * (q_rows @ kbar)"),
+    ("stand_in_without_scale", "logits[:, n] = sigma * (q_rows @ kbar) + math.log(c1 - c0)",
+     "logits[:, n] = q_rows @ kbar + math.log(c1 - c0)"),
+    ("stand_ins_for_kept_blocks", "if not kept and block_class(i, j, Bq, Bk, L) == CANDIDATE]",
+     "if block_class(i, j, Bq, Bk, L) == CANDIDATE]"),
+    ("stand_in_value_first_row", "vbar[n] = v_h[c0:c1].mean(axis=0)", "vbar[n] = v_h[c0]"),
+    ("stand_in_key_first_row", "kbar = k_h[c0:c1].mean(axis=0)", "kbar = k_h[c0]"),
+    # packing and accounting
+    ("varlen_drops_last_sequence", "for b in range(len(cu_seqlens) - 1):",
+     "for b in range(len(cu_seqlens) - 2):"),
+    ("flops_without_pv",
+     "return F * (float(np.count_nonzero(visible)) + float(np.count_nonzero(keep)))",
+     "return F * float(np.count_nonzero(visible))"),
+]
+
+ORACLE_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                           "oracle", "bsfa_oracle.py")
+
+
+def mutated_source(name: str) -> str:
+    """The oracle's source with mutant ``name`` applied."""
+    entry = [m for m in MUTANTS if m[0] == name]
+    if len(entry) != 1:
+        raise KeyError(name)
+    _, old, new = entry[0]
+    with open(ORACLE_PATH) as f:
+        src = f.read()
+    if src.count(old) != 1:
+        raise ValueError(f"mutant {name}: the original text occurs {src.count(old)} times")
+    return src.replace(old, new)
+
+
+def _install(name: str) -> None:
+    import oracle
+    mod = types.ModuleType("oracle.bsfa_oracle")
+    mod.__file__ = ORACLE_PATH
+    mod.__package__ = "oracle"
+    sys.modules["oracle.bsfa_oracle"] = mod
+    exec(compile(mutated_source(name), ORACLE_PATH, "exec"), mod.__dict__)
+    oracle.bsfa_oracle = mod
+
+
+if os.environ.get(ENV):
+    _install(os.environ[ENV])

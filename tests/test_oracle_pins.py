@@ -329,24 +329,62 @@ def test_order_invariance_against_streaming(seed):
 # Structural equivalences
 # ---------------------------------------------------------------------------
 def test_last_position_reuse():
+    """Query blocks past the calibrated length take the last threshold (Key
+    Designs 1): a short table equals the same table padded with copies of its
+    last entry, at thresholds that skip some blocks and keep others."""
     Hq, L, d, B = 2, 64, 8, 8
     q, k, v = _rand((Hq, L, d), 90), _rand((Hq, L, d), 91), _rand((Hq, L, d), 92)
-    T_short = _rand((Hq, 3), 93) * 0.2 + 1.0
+    T_short = _rand((Hq, 3), 93) * 0.3 + 2.4  # around the maxima of 8 x 8 N(0, 1) tiles
     T_long = np.concatenate([T_short, np.repeat(T_short[:, -1:], 5, axis=1)], axis=1)
     a = orc.prefill(q, k, v, Bq=B, Bk=B, thresholds=T_short)
     b = orc.prefill(q, k, v, Bq=B, Bk=B, thresholds=T_long)
+    late = a["candidate"][:, 3:]
+    assert 0 < a["keep"][:, 3:][late].sum() < late.sum()  # reuse decides something
     assert np.array_equal(a["keep"], b["keep"])
     assert np.array_equal(a["out"], b["out"])
+
+
+def test_last_position_reuse_closed_form():
+    """T = [-inf, -inf, +inf] over 8 query blocks: blocks 0 and 1 attend
+    densely, every later block (reusing +inf) only to its diagonal block."""
+    Hq, L, d, B = 1, 64, 8, 8
+    q, k, v = _rand((Hq, L, d), 94), _rand((Hq, L, d), 95), _rand((Hq, L, d), 96)
+    sigma = 1 / math.sqrt(d)
+    T = np.array([[-np.inf, -np.inf, np.inf]])
+    r = orc.prefill(q, k, v, Bq=B, Bk=B, sigma=sigma, thresholds=T)
+    mask = np.array([[c <= rr and (rr < 2 * B or c // B == rr // B) for c in range(L)]
+                     for rr in range(L)])
+    assert np.max(np.abs(r["out"] - _sdpa(q, k, v, mask=mask, sigma=sigma))) < 1e-12
 
 
 def test_gqa_equals_repeated_kv():
     Hq, Hkv, L, d, B = 4, 2, 40, 8, 8
     q, k, v = _rand((Hq, L, d), 94), _rand((Hkv, L, d), 95), _rand((Hkv, L, d), 96)
-    T = _rand((Hq, 5), 97) * 0.2 + 1.0
+    T = _rand((Hq, 5), 97) * 0.3 + 2.4  # around the maxima of 8 x 8 N(0, 1) tiles
     a = orc.prefill(q, k, v, Bq=B, Bk=B, thresholds=T)
     b = orc.prefill(q, _repeat_kv(k, 2), _repeat_kv(v, 2), Bq=B, Bk=B, thresholds=T)
+    assert 0 < a["keep"][a["candidate"]].sum() < a["candidate"].sum()
     assert np.array_equal(a["keep"], b["keep"])
     assert np.array_equal(a["out"], b["out"])
+
+
+def test_thresholds_are_indexed_by_query_head():
+    """Under GQA each query head reads its own threshold row and the KV head
+    h // (Hq / Hkv): rows alternating -inf / +inf make the even query heads
+    dense and the odd ones diagonal-only (library SDPA for both)."""
+    Hq, Hkv, L, d, B = 4, 2, 40, 8, 8
+    q, k, v = _rand((Hq, L, d), 110), _rand((Hkv, L, d), 111), _rand((Hkv, L, d), 112)
+    sigma = 1 / math.sqrt(d)
+    T = np.array([[-np.inf], [np.inf], [-np.inf], [np.inf]])
+    r = orc.prefill(q, k, v, Bq=B, Bk=B, sigma=sigma, thresholds=T)
+    diag = np.array([[c <= rr and c // B == rr // B for c in range(L)] for rr in range(L)])
+    for h in range(Hq):
+        kh = h // 2
+        if h % 2 == 0:
+            ref = _sdpa(q[h:h + 1], k[kh:kh + 1], v[kh:kh + 1], causal=True, sigma=sigma)
+        else:
+            ref = _sdpa(q[h:h + 1], k[kh:kh + 1], v[kh:kh + 1], mask=diag, sigma=sigma)
+        assert np.max(np.abs(r["out"][h] - ref[0])) < 1e-12, f"head {h}"
 
 
 def test_varlen_equals_separate_calls():

@@ -100,8 +100,11 @@ typedef enum {
    * unchanged.  The block means are computed in fp32 from K and V and stored in
    * the element type in the workspace (bsfa_prefill_workspace_size includes
    * them).  Requires block_q == block_k == 128, contiguous K/V (block_table
-   * NULL), no BSFA_FLAG_V_ALWAYS and sequences of at most 524288 tokens; else
-   * BSFA_ERR_UNSUPPORTED. */
+   * NULL), no BSFA_FLAG_V_ALWAYS, sequences of at most 524288 tokens and
+   * head_dim * num_heads_kv <= 1024 (one thread per element in the block-mean
+   * pass: Hkv <= 8 at d = 128, <= 16 at d = 64); else BSFA_ERR_UNSUPPORTED.
+   * The last limit is checked after the scheduling pre-pass has been queued
+   * on the stream (it only writes the workspace). */
   BSFA_FLAG_MEAN_CORRECTION = 2
 } bsfa_flag;
 

@@ -122,3 +122,29 @@ def test_fp16_corrected_matches_oracle(cuda_device):
     bits, _ = gu.unpack_bitmap(r["bitmap"], Hq, [L], B, B)
     assert np.array_equal(bits[0], ref["keep"])
     gu.assert_close(gu.to64(r["out"][0]), ref["out"], "out", max_abs=4e-3, mean_abs=4e-4)
+
+
+def test_block_mean_pass_head_limit(cuda_device):
+    """The block-mean pass takes one thread per (KV head, element): d * Hkv <=
+    1024.  16 KV heads run at d = 64 (against the oracle) and are refused with
+    BSFA_ERR_UNSUPPORTED at d = 128, leaving the device clean."""
+    b = _bsfa()
+    Hq = Hkv = 16
+    L = 300
+    T = torch.full((Hq, 1), 0.5, device=cuda_device)
+    x = wl.layer_inputs(Hq, Hkv, L, 64, 460, skip_rate=0.5)
+    r = _run(x.q.to(cuda_device)[None], x.k.to(cuda_device)[None], x.v.to(cuda_device)[None],
+             mode="threshold", thresholds=T, mean_correction=True)
+    ref = orc.prefill(gu.to64(x.q), gu.to64(x.k), gu.to64(x.v), Bq=B, Bk=B,
+                      thresholds=np.full((Hq, 1), 0.5), mean_correction=True)
+    bits, _ = gu.unpack_bitmap(r["bitmap"], Hq, [L], B, B)
+    assert np.array_equal(bits[0], ref["keep"])
+    gu.assert_close(gu.to64(r["out"][0]), ref["out"], "out")
+    x = wl.layer_inputs(Hq, Hkv, L, 128, 461, skip_rate=0.5)
+    with pytest.raises(b.BsfaError) as e:
+        b.prefill(x.q.to(cuda_device)[None], x.k.to(cuda_device)[None],
+                  x.v.to(cuda_device)[None], mode="threshold", thresholds=T,
+                  mean_correction=True)
+    assert e.value.status == 2
+    torch.cuda.synchronize()
+    assert b.api.device_error() == 0

@@ -44,12 +44,16 @@ constexpr int KST = 2;  // K ring stages
 constexpr int CORR_WORDS = 128;
 constexpr int VST = 2;  // V ring stages
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
+// Lazy rescale: P is taken against a maximum that may trail the true running
+// maximum by up to 8 in log2 units (P entries up to 2^8); only a larger rise
+// rescales O and l.
 constexpr float RESCALE_LOG2 = 8.0f;
-// Decision words carry the tile counter above the four decision bits, so a
-// reader can tell a published decision from the word of two tiles earlier.
+// Decision words carry the tile counter (its low 28 bits) above the four
+// decision bits, so a reader can tell a published decision from the word of
+// two tiles earlier.
 constexpr uint32_t DEC_BITS = 4;
 constexpr uint32_t DEC_MASK = (1u << DEC_BITS) - 1u;
-constexpr uint32_t DEC_STAMP_MASK = 0x0FFFFFFFu;  // lazy rescale: P may grow to 2^8 before O is rescaled
+constexpr uint32_t DEC_STAMP_MASK = 0x0FFFFFFFu;
 // Register split for two slots (384 threads): warpgroup 0 (copies, MMA issue)
 // drops to COPY_REGS, the two softmax warpgroups rise to SOFTMAX_REGS.  The
 // host checks 128*COPY_REGS + 256*SOFTMAX_REGS against the registers the

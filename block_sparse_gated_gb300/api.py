@@ -213,6 +213,11 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
     candidates, diagonal-region blocks).  ``v_always`` loads V for skipped
     tiles too (results unchanged; for measuring what the skipped load saves).
 
+    cu_seqlens must be non-decreasing from 0 or more, end at no more than
+    the packed token count, and no length may exceed ``max_seqlen``: the
+    offsets stay on the device and are not checked (that would need a
+    synchronisation per call).
+
     Paged K/V: with ``block_table`` (int32 [batch, pages_per_sequence] on the
     device), k and v are page pools [pages, page_size, Hkv, d] (``kv_layout``
     "pthd") or [pages, Hkv, page_size, d] ("phtd"), page_size a multiple of

@@ -117,6 +117,11 @@ typedef enum {
  *   - varlen   (cu_seqlens != NULL): `batch` sequences packed along tokens,
  *     `seqlen` = total packed tokens, sequence b owns tokens
  *     [cu_seqlens[b], cu_seqlens[b+1]); the batch stride is ignored.
+ *     cu_seqlens lives in device memory and is read by the kernels only, so
+ *     the library cannot check it without a synchronisation: the caller
+ *     guarantees 0 <= cu_seqlens[0] <= cu_seqlens[1] <= ... <=
+ *     cu_seqlens[batch] <= seqlen and every length <= max_seqlen.  Offsets
+ *     that break this make the kernels read and write out of bounds.
  * Strides must be multiples of 8 elements (16 bytes) and the base pointers
  * 16-byte aligned (TMA requirement).  q-head h reads KV head h / (Hq/Hkv).
  */

@@ -89,7 +89,7 @@ def layer_inputs(Hq: int, Hkv: int, L: int, d: int, seed: int, device="cpu", *,
         gen = _gen(seed, _STREAM_SCALE, "cpu")
         uni = torch.rand((Hkv, nk), generator=gen)
         skip_tier = uni < skip_rate
-        skip_tier[:, 0] = False
+        skip_tier[:, :1] = False  # block 0 keeps scale 1 (no blocks when L = 0)
         scale = torch.where(skip_tier, torch.tensor(skip_scale), torch.tensor(1.0))
         scale_tok = scale.repeat_interleave(block, dim=1)[:, :L].to(device)
         k *= scale_tok[:, :, None]

@@ -49,3 +49,46 @@ def test_two_million_token_sequence(cuda_device):
         gu.assert_close(gu.to64(out[r0:r1]), ref["out"], f"out block {i}")
         gu.assert_close(gu.to64(lse[r0:r1]), ref["lse"], f"lse block {i}", max_abs=gu.LSE_ABS,
                         mean_abs=gu.LSE_ABS)
+
+
+def test_most_sequences_per_call(cuda_device):
+    """The largest accepted batch: 4096 packed sequences (lengths 0-400,
+    seeded) of 64-row / 64-key semantic blocks in one varlen call.  Block
+    counts are checked against their closed form over every sequence, the
+    bitmap rows are clean past each sequence's last key block, and sampled
+    sequences (including the first and the last) against the oracle."""
+    import block_sparse_gated_gb300 as bsfa
+    Hq, Hkv, d, Bs, n_seq = 2, 1, 64, 64, 4096
+    lens = np.random.default_rng(920).integers(0, 401, size=n_seq).tolist()
+    lens[0], lens[-1], lens[7] = 400, 1, 0
+    parts = [wl.layer_inputs(Hq, Hkv, Ln, d, 921 + n, skip_rate=0.5, block=Bs) for n, Ln in
+             enumerate(lens)]
+    q, cu = wl.pack_varlen([p.q for p in parts])
+    k, _ = wl.pack_varlen([p.k for p in parts])
+    v, _ = wl.pack_varlen([p.v for p in parts])
+    T = torch.full((Hq, 1), 1.0, device=cuda_device)
+    r = bsfa.prefill(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                     cu_seqlens=cu.to(cuda_device), max_seqlen=max(lens), block_q=Bs, block_k=Bs,
+                     mode="threshold", thresholds=T, return_bitmap=True, return_lse=True,
+                     return_counts=True)
+    torch.cuda.synchronize()
+    assert bsfa.api.device_error() == 0
+    nb = [orc.num_blocks(Ln, Bs) for Ln in lens]
+    kept, cand, diag = r["counts"].cpu().tolist()
+    assert cand == Hq * sum(n * (n - 1) // 2 for n in nb) and diag == Hq * sum(nb)
+    assert 0 < kept < cand
+    bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, lens, Bs, Bs)
+    assert clean
+    sigma = 1.0 / math.sqrt(d)
+    cu_l = cu.tolist()
+    picks = [0, 7, n_seq - 1] + np.random.default_rng(922).choice(n_seq, 13, replace=False).tolist()
+    for b in picks:
+        a, e = cu_l[b], cu_l[b + 1]
+        if e == a:
+            continue
+        ref = orc.prefill(gu.to64(q[:, a:e]), gu.to64(k[:, a:e]), gu.to64(v[:, a:e]), Bq=Bs,
+                          Bk=Bs, sigma=sigma, thresholds=np.full((Hq, 1), 1.0))
+        assert np.array_equal(bits[b], ref["keep"]), f"bitmap of sequence {b}"
+        gu.assert_close(gu.to64(r["out"][:, a:e]), ref["out"], f"out of sequence {b}")
+        gu.assert_close(gu.to64(r["lse"][:, a:e]), ref["lse"], f"lse of sequence {b}",
+                        max_abs=gu.LSE_ABS, mean_abs=gu.LSE_ABS)

@@ -6,7 +6,6 @@ provides device memory and the current stream.
 from __future__ import annotations
 
 import ctypes
-import math
 
 import torch
 
@@ -27,10 +26,6 @@ class BsfaError(RuntimeError):
 def _check(status: int, what: str = ""):
     if status != 0:
         raise BsfaError(status, what)
-
-
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream, device=None):
@@ -336,6 +331,3 @@ def device_error(stream=None) -> int:
         _check(st, "bsfa_device_error")
     return int(code.value)
 
-
-def default_scale(d: int) -> float:
-    return 1.0 / math.sqrt(d)

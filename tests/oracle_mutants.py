@@ -22,6 +22,8 @@ MUTANTS = [
     # block geometry and the score matrix
     ("partial_blocks_as_candidates", "if (j + 1) * Bk <= first_row:",
      "if j * Bk <= first_row:"),
+    ("candidate_when_fully_visible", "if (j + 1) * Bk <= first_row:",
+     "if (j + 1) * Bk - 1 <= first_row:"),
     ("last_row_window_shrinks", "if first_key <= last_row:", "if first_key < last_row:"),
     ("causal_mask_excludes_self", "s = np.where(cols[None, :] <= rows[:, None], s, NEG_INF)",
      "s = np.where(cols[None, :] < rows[:, None], s, NEG_INF)"),

@@ -233,7 +233,7 @@ def _brute_block_max(s, i, j, Bq, Bk, L):
                for c in range(j * Bk, min((j + 1) * Bk, L)) if c <= r)
 
 
-@pytest.mark.parametrize("Bq,Bk,L", [(3, 3, 20), (4, 2, 19), (2, 4, 21)])
+@pytest.mark.parametrize("Bq,Bk,L", [(3, 3, 20), (4, 2, 19), (2, 4, 21), (3, 2, 23)])
 def test_threshold_keep_set_brute_force(Bq, Bk, L):
     d = 3
     q, k, v = _rand((1, L, d), 17), _rand((1, L, d), 18), _rand((1, L, d), 19)

@@ -287,3 +287,16 @@ def test_binding_checks_shapes_the_library_cannot_see():
     with pytest.raises(ValueError, match="block_table"):
         api._params(qv, pool, pool, qv, block_table=torch.zeros(2, 1, dtype=torch.int32),
                     **dict(kw, cu_seqlens=cu, max_seqlen=200))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: without the built library the first call raises."""
+    import torch
+    from block_sparse_gated_gb300 import _native, api
+    monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "libbsfa.so"))
+    monkeypatch.setattr(_native, "_lib", None)
+    with pytest.raises(RuntimeError, match="is not built"):
+        _native.lib()
+    with pytest.raises(RuntimeError, match="is not built"):
+        api.prefill_workspace_bytes(*(torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16),) * 3,
+                                    mode="none")

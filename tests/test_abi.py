@@ -300,3 +300,44 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     with pytest.raises(RuntimeError, match="is not built"):
         api.prefill_workspace_bytes(*(torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16),) * 3,
                                     mode="none")
+
+
+def test_plain_c_caller_links_and_gets_host_statuses(libpath):
+    """The boundary is usable from C alone: a C program built with gcc against
+    include/bsfa.h and linked to the library gets sizes, words per row and
+    host-side statuses back (no device work)."""
+    import tempfile
+    src = r'''
+#include <stdio.h>
+#include <string.h>
+#include "bsfa.h"
+int main(void) {
+  bsfa_fwd_params p;
+  memset(&p, 0, sizeof p);
+  p.batch = 2; p.num_heads_q = 4; p.num_heads_kv = 2; p.seqlen = 1000; p.head_dim = 128;
+  p.block_q = 128; p.block_k = 64; p.mode = BSFA_GATE_NONE;
+  int words = -1;
+  int st_words = bsfa_bitmap_words_per_row(&p, &words);
+  size_t ws = bsfa_prefill_workspace_size(&p);
+  p.head_dim = 96;
+  int st_d96 = bsfa_prefill_fwd(&p, NULL);
+  p.head_dim = 128; p.batch = 0;
+  int st_empty = bsfa_prefill_fwd(&p, NULL);
+  printf("%d %d %d %zu %d %d %s\n", bsfa_version() > 0, st_words, words, ws, st_d96, st_empty,
+         bsfa_status_string(BSFA_ERR_WORKSPACE));
+  return 0;
+}
+'''
+    libdir = os.path.dirname(libpath)
+    with tempfile.TemporaryDirectory() as tmp:
+        c = os.path.join(tmp, "caller.c")
+        exe = os.path.join(tmp, "caller")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe, libpath,
+                        f"-Wl,-rpath,{libdir}"], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()
+    ok, st_words, words, ws, st_d96, st_empty = map(int, out[:6])
+    assert ok == 1 and st_words == 0 and words == 1  # ceil(ceil(1000 / 64) / 32) = 1
+    assert ws > 0
+    assert st_d96 == 2 and st_empty == 0  # unsupported head_dim; an empty batch is a no-op
+    assert " ".join(out[6:]) == "workspace missing, misaligned or too small"

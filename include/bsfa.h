@@ -24,11 +24,15 @@
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers unless a parameter says "host".
  *     The caller owns every buffer; the library never allocates device memory
- *     (scratch comes from the caller's workspace).
+ *     at run time (scratch comes from the caller's workspace).  Its only
+ *     device memory of its own is static: the device error word and the
+ *     fixed scratch array of bsfa_prefill_fwd_noalloc.
  *   - Calls are asynchronous on `stream` and never synchronise the host,
  *     except bsfa_device_error which synchronises `stream` by design.
  *   - Errors that the host can detect are returned before anything is
- *     launched.  A device-side wait that ran out of time (a hang guard, never
+ *     launched, with one exception: the mean-correction head limit
+ *     (BSFA_FLAG_MEAN_CORRECTION) is returned after the scheduling pre-pass
+ *     has been queued, which writes only the workspace.  A device-side wait that ran out of time (a hang guard, never
  *     expected in a correct run) sets a device error word; it is reported by
  *     bsfa_device_error.
  *   - No C++ exception crosses this boundary.
@@ -201,8 +205,10 @@ size_t bsfa_prefill_workspace_size(const bsfa_fwd_params* p);
 bsfa_status bsfa_bitmap_words_per_row(const bsfa_fwd_params* p, int* words_per_row);
 
 /* Gated causal prefill.  Validates `p`, then enqueues on `stream` a small
- * scheduling kernel and the persistent attention kernel.  Asynchronous.
- * Errors: BSFA_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE before any launch;
+ * scheduling kernel, the block-mean kernel when BSFA_FLAG_MEAN_CORRECTION is
+ * set, and the persistent attention kernel.  Asynchronous.
+ * Errors: BSFA_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE before any launch
+ * (except the mean-correction head limit, see BSFA_FLAG_MEAN_CORRECTION);
  * BSFA_ERR_CUDA if a launch or descriptor encode fails. */
 bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream);
 

@@ -63,3 +63,36 @@ def test_skip_tier_scales_whole_key_blocks_and_spares_block_zero():
             blk, ref = x.k[kh, j * 128:(j + 1) * 128].float(), plain.k[kh, j * 128:(j + 1) * 128].float()
             r = float(blk.norm() / ref.norm())
             assert abs(r - (0.01 if x.skip_tier[kh, j] else 1.0)) < 0.01 * (0.01 if x.skip_tier[kh, j] else 1.0) + 1e-3
+
+
+def test_workload_shapes_and_visible_tiles():
+    """The five benchmark workloads keep their stated shapes, and their
+    visible-tile counts (counted block by block with the oracle's geometry)
+    equal the closed form Hq * sum_b n_b (n_b + 1) / 2: 272 for the tiny case,
+    1,052,672 at 32K, 16,793,600 at 128K, 4,202,496 at 64K and 8,710,144 per
+    layer for the 8-sequence batch."""
+    from oracle import bsfa_oracle as orc
+    W = wl.WORKLOADS
+    assert (W["tiny-h2-d64-L1024"]["Hq"], W["tiny-h2-d64-L1024"]["d"],
+            W["tiny-h2-d64-L1024"]["L"], W["tiny-h2-d64-L1024"]["Bq"]) == (2, 64, 1024, 64)
+    for name in ("llama8b-L32768", "llama8b-L131072", "lambda-sweep-L65536",
+                 "varlen-8seq-32layer"):
+        c = W[name]
+        assert (c["Hq"], c["Hkv"], c["d"], c["Bq"], c["Bk"]) == (32, 8, 128, 128, 128), name
+    assert W["llama8b-L131072"]["ks"] == [32, 128, 512]
+    assert W["llama8b-L131072"]["cal_L"] == 65536
+    assert W["varlen-8seq-32layer"]["lens"] == [n * 1024 for n in (4, 8, 12, 16, 24, 32, 48, 64)]
+    stated = {"tiny-h2-d64-L1024": 272, "llama8b-L32768": 1_052_672,
+              "llama8b-L131072": 16_793_600, "lambda-sweep-L65536": 4_202_496,
+              "varlen-8seq-32layer": 8_710_144}
+    for name, want in stated.items():
+        c = W[name]
+        lens = c.get("lens", [c.get("L")])
+        per_head = 0
+        for Ln in lens:
+            n = orc.num_blocks(Ln, c["Bq"])
+            per_head += sum(1 for i in range(n) for j in range(orc.num_blocks(Ln, c["Bk"]))
+                            if orc.block_class(i, j, c["Bq"], c["Bk"], Ln) is not None)
+        assert c["Hq"] * per_head == want, name
+        assert want == c["Hq"] * sum(orc.num_blocks(Ln, c["Bq"]) * (orc.num_blocks(Ln, c["Bq"]) + 1)
+                                     // 2 for Ln in lens)

@@ -6,11 +6,15 @@ term, a wrong index, a swapped visiting order.  The original text must occur
 exactly once in the oracle's source, so a mutant that no longer applies is an
 error rather than a silent pass.
 
+``GUARD_MUTANTS`` does the same for ``oracle/guard.py``, the guard band that
+keeps generated thresholds clear of ties; its pins are
+``tests/test_oracle_guard.py``.
+
 Loaded as a pytest plugin (``-p tests.oracle_mutants``) with the environment
 variable ``BSFA_ORACLE_MUTANT`` naming one entry, it builds that mutant of the
-oracle module on the CPU and installs it in place of ``oracle.bsfa_oracle``
-for the test session; the oracle's file is not touched.  Without the variable
-it does nothing.
+module on the CPU and installs it in place of ``oracle.bsfa_oracle`` (or
+``oracle.guard``) for the test session; the files are not touched.  Without
+the variable it does nothing.
 """
 import os
 import sys
@@ -90,17 +94,40 @@ MUTANTS = [
      "return F * float(np.count_nonzero(visible))"),
 ]
 
-ORACLE_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                           "oracle", "bsfa_oracle.py")
+GUARD_MUTANTS = [
+    ("guard_gqa_modulo", "c = orc.candidate_maxima(qs[h], ks_[h // g], i, Bq, Bk, sigma)",
+     "c = orc.candidate_maxima(qs[h], ks_[h % Hkv], i, Bq, Bk, sigma)"),
+    ("guard_keys_without_reuse",
+     "out.setdefault((h, orc.threshold_index(i, nT)), []).extend(c)",
+     "out.setdefault((h, i), []).extend(c)"),
+    ("guard_any_gap", "idx = np.nonzero(gaps >= min_gap)[0]", "idx = np.nonzero(gaps > 0)[0]"),
+    ("guard_no_low_end", "cands = [vals[0] - margin, vals[-1] + margin]",
+     "cands = [vals[-1] + margin]"),
+    ("guard_moves_clear_values",
+     "if vals.size == 0 or not np.any(np.abs(vals - x) < band):", "if vals.size == 0:"),
+]
+
+_ORACLE_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
+ORACLE_PATH = os.path.join(_ORACLE_DIR, "bsfa_oracle.py")
+GUARD_PATH = os.path.join(_ORACLE_DIR, "guard.py")
+
+
+def target(name: str):
+    """(module name under ``oracle``, source path, pin file) of mutant ``name``."""
+    if any(m[0] == name for m in MUTANTS):
+        return "bsfa_oracle", ORACLE_PATH, "tests/test_oracle_pins.py"
+    if any(m[0] == name for m in GUARD_MUTANTS):
+        return "guard", GUARD_PATH, "tests/test_oracle_guard.py"
+    raise KeyError(name)
 
 
 def mutated_source(name: str) -> str:
-    """The oracle's source with mutant ``name`` applied."""
-    entry = [m for m in MUTANTS if m[0] == name]
+    """The target module's source with mutant ``name`` applied."""
+    entry = [m for m in MUTANTS + GUARD_MUTANTS if m[0] == name]
     if len(entry) != 1:
         raise KeyError(name)
     _, old, new = entry[0]
-    with open(ORACLE_PATH) as f:
+    with open(target(name)[1]) as f:
         src = f.read()
     if src.count(old) != 1:
         raise ValueError(f"mutant {name}: the original text occurs {src.count(old)} times")
@@ -109,12 +136,13 @@ def mutated_source(name: str) -> str:
 
 def _install(name: str) -> None:
     import oracle
-    mod = types.ModuleType("oracle.bsfa_oracle")
-    mod.__file__ = ORACLE_PATH
+    mod_name, path, _ = target(name)
+    mod = types.ModuleType(f"oracle.{mod_name}")
+    mod.__file__ = path
     mod.__package__ = "oracle"
-    sys.modules["oracle.bsfa_oracle"] = mod
-    exec(compile(mutated_source(name), ORACLE_PATH, "exec"), mod.__dict__)
-    oracle.bsfa_oracle = mod
+    sys.modules[f"oracle.{mod_name}"] = mod
+    exec(compile(mutated_source(name), path, "exec"), mod.__dict__)
+    setattr(oracle, mod_name, mod)
 
 
 if os.environ.get(ENV):

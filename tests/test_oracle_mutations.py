@@ -1,8 +1,8 @@
 """The oracle's pins catch plausible mistakes in it.
 
 For every planted mistake in ``tests/oracle_mutants.py`` the pin suite
-(``tests/test_oracle_pins.py``) runs in a child process against the mutated
-oracle and must fail; a mutant that every pin lets through is a mistake the
+(``tests/test_oracle_pins.py``, or ``tests/test_oracle_guard.py`` for the
+guard band) runs in a child process against the mutated module and must fail; a mutant that every pin lets through is a mistake the
 pins cannot see.  The unmutated oracle passing the same suite is the normal
 CPU run.  No GPU involved."""
 import os
@@ -17,16 +17,18 @@ from tests import oracle_mutants as om
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+ALL = [m[0] for m in om.MUTANTS + om.GUARD_MUTANTS]
+
+
 def test_every_mutant_applies_to_the_current_oracle():
-    for name, _, _ in om.MUTANTS:
-        src = om.mutated_source(name)
-        compile(src, om.ORACLE_PATH, "exec")
-    assert len({m[0] for m in om.MUTANTS}) == len(om.MUTANTS)
+    for name in ALL:
+        compile(om.mutated_source(name), om.target(name)[1], "exec")
+    assert len(set(ALL)) == len(ALL)
 
 
 def _run_pins(name):
     env = dict(os.environ, **{om.ENV: name})
-    cmd = [sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-x", "-q",
+    cmd = [sys.executable, "-m", "pytest", om.target(name)[2], "-x", "-q",
            "-p", "tests.oracle_mutants", "-p", "no:cacheprovider"]
     return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
@@ -36,10 +38,10 @@ def pin_runs():
     """The pin suite against every mutant, several child processes at a time."""
     workers = max(1, min(8, (os.cpu_count() or 2) // 2))
     with ThreadPoolExecutor(workers) as ex:
-        return dict(zip([m[0] for m in om.MUTANTS], ex.map(_run_pins, [m[0] for m in om.MUTANTS])))
+        return dict(zip(ALL, ex.map(_run_pins, ALL)))
 
 
-@pytest.mark.parametrize("name", [m[0] for m in om.MUTANTS])
+@pytest.mark.parametrize("name", ALL)
 def test_pins_catch_mutant(name, pin_runs):
     r = pin_runs[name]
     tail = "\n".join(r.stdout.splitlines()[-15:])

@@ -160,12 +160,11 @@ def visit_order_ascending(i: int, Bq: int, Bk: int, L: int) -> list[int]:
 
 
 def keep_lambda(s: np.ndarray, i: int, Bq: int, Bk: int, L: int,
-                log_lambda: float, order: Sequence[int] | None = None,
-                trace: list | None = None) -> dict[int, bool]:
+                log_lambda: float, trace: list | None = None) -> dict[int, bool]:
     """lambda-relative gate ("Vote, then skip").
 
-    Blocks are visited in ``order`` (default: ascending key position, the
-    diagonal region last).  Each row r keeps an exact running max m_r over the
+    Blocks are visited in ascending key position, the diagonal region last
+    (``visit_order_ascending``).  Each row r keeps an exact running max m_r over the
     scores of the blocks kept so far, starting at -inf.  A candidate block is
     skipped iff rowmax_r - m_r < ln(lambda) for every row r of the query
     block; one row at or above the bound keeps it.  A kept block raises m_r to
@@ -173,8 +172,7 @@ def keep_lambda(s: np.ndarray, i: int, Bq: int, Bk: int, L: int,
     region is always kept.
 
     If ``trace`` is a list, (j, m_before, rowmax, kept) tuples are appended."""
-    if order is None:
-        order = visit_order_ascending(i, Bq, Bk, L)
+    order = visit_order_ascending(i, Bq, Bk, L)
     m = np.full(s.shape[0], NEG_INF)
     keep = {}
     for j in order:
@@ -196,15 +194,18 @@ def keep_lambda(s: np.ndarray, i: int, Bq: int, Bk: int, L: int,
     return keep
 
 
-def decision_statistics(q_h, k_h, i, Bq, Bk, sigma, order=None,
-                        log_lambda=NEG_INF):
-    """For lambda mode: the per-candidate statistic max_r(rowmax_r - m_r) at
-    visit time, under the keep decisions that ``log_lambda`` produces.  Used to
-    keep generated inputs clear of the decision boundary."""
+def decision_statistics(q_h, k_h, i, Bq, Bk, sigma, log_lambda=NEG_INF):
+    """For lambda mode: the per-candidate statistic max_r(rowmax_r - m_r),
+    with m_r the running max as it stands when block j is visited (before
+    block j can raise it), under the keep decisions that ``log_lambda``
+    produces.  Block j is kept exactly when its statistic is >= ln(lambda).
+    Used to keep generated inputs clear of the decision boundary.
+
+    Returns [(j, statistic)] in visiting order, candidates only."""
     s, _ = query_block_scores(q_h, k_h, i, Bq, sigma)
     L = q_h.shape[0]
     trace: list = []
-    keep_lambda(s, i, Bq, Bk, L, log_lambda, order, trace)
+    keep_lambda(s, i, Bq, Bk, L, log_lambda, trace)
     out = []
     for j, m_before, rowmax, kept in trace:
         if block_class(i, j, Bq, Bk, L) != CANDIDATE:
@@ -267,12 +268,10 @@ def mean_stand_ins(q_rows: np.ndarray, k_h: np.ndarray, v_h: np.ndarray,
 # One query block, one head: the unit everything else loops over.
 # ---------------------------------------------------------------------------
 def query_block(q_h, k_h, v_h, i, *, Bq, Bk, sigma, mode, T_hi=None,
-                log_lambda=None, order=None, keep_override=None, mean_correction=False):
+                log_lambda=None, mean_correction=False):
     """Gated attention for query block i of one head.
 
     mode: "threshold", "lambda" or "dense" (every visible block kept).
-    keep_override: optional {j: bool} that replaces the decisions for the
-    listed candidate blocks (used by tests to evaluate a given keep set).
     mean_correction: add the mean stand-in of every skipped candidate block.
 
     Returns dict(out [rows, d], lse [rows], keep {j: bool}, smax {j: float})."""
@@ -281,16 +280,12 @@ def query_block(q_h, k_h, v_h, i, *, Bq, Bk, sigma, mode, T_hi=None,
     if mode == "threshold":
         keep = keep_threshold(s, i, Bq, Bk, L, T_hi)
     elif mode == "lambda":
-        keep = keep_lambda(s, i, Bq, Bk, L, log_lambda, order)
+        keep = keep_lambda(s, i, Bq, Bk, L, log_lambda)
     elif mode == "dense":
         keep = {j: True for j in range(num_blocks(s.shape[1], Bk))
                 if block_class(i, j, Bq, Bk, L) is not None}
     else:
         raise ValueError(mode)
-    if keep_override:
-        for j, kept in keep_override.items():
-            if block_class(i, j, Bq, Bk, L) == CANDIDATE:
-                keep[j] = bool(kept)
     smax = {j: tile_max(s, j, Bk) for j in keep}
     stand_in = None
     if mean_correction:
@@ -306,13 +301,12 @@ def _kv_head(h: int, Hq: int, Hkv: int) -> int:
 
 
 def prefill(q, k, v, *, Bq, Bk, sigma=None, mode="threshold",
-            thresholds=None, log_lambda=None, order_fn=None, blocks=None,
+            thresholds=None, log_lambda=None, blocks=None,
             mean_correction=False):
     """Gated causal prefill of one sequence.
 
     q: [Hq, L, d]; k, v: [Hkv, L, d] (float64 or anything np.float64 takes).
     thresholds: [Hq, nT] (threshold mode).  sigma defaults to 1/sqrt(d).
-    order_fn(h, i) -> visit order (lambda mode only; default ascending).
     blocks: optional iterable of (h, i) to evaluate; others are left NaN.
     mean_correction: add the mean stand-ins of skipped candidate blocks.
 
@@ -337,9 +331,8 @@ def prefill(q, k, v, *, Bq, Bk, sigma=None, mode="threshold",
         T_hi = None
         if mode == "threshold":
             T_hi = float(thresholds[h][threshold_index(i, len(thresholds[h]))])
-        order = order_fn(h, i) if (order_fn is not None and mode == "lambda") else None
         res = query_block(q[h], k[kh], v[kh], i, Bq=Bq, Bk=Bk, sigma=sigma,
-                          mode=mode, T_hi=T_hi, log_lambda=log_lambda, order=order,
+                          mode=mode, T_hi=T_hi, log_lambda=log_lambda,
                           mean_correction=mean_correction)
         r0, r1 = i * Bq, min((i + 1) * Bq, L)
         out[h, r0:r1] = res["out"]

@@ -76,6 +76,15 @@ MUTANTS = [
     ("lambda_tile_max_statistic", "rowmax = np.max(s[:, j * Bk:(j + 1) * Bk], axis=1)",
      "rowmax = np.full(s.shape[0], np.max(s[:, j * Bk:(j + 1) * Bk]))"),
     ("lambda_descending", "return cands + diags", "return cands[::-1] + diags"),
+    ("lambda_statistic_after_update",
+     "        if trace is not None:\n            trace.append((j, m.copy(), rowmax.copy(), kept))\n"
+     "        keep[j] = kept\n        if kept:\n            m = np.maximum(m, rowmax)",
+     "        keep[j] = kept\n        if kept:\n            m = np.maximum(m, rowmax)\n"
+     "        if trace is not None:\n            trace.append((j, m.copy(), rowmax.copy(), kept))"),
+    ("lambda_statistic_min_over_rows", "out.append((j, float(np.max(rowmax - m_before))))",
+     "out.append((j, float(np.min(rowmax - m_before))))"),
+    ("lambda_statistic_tile_wide", "out.append((j, float(np.max(rowmax - m_before))))",
+     "out.append((j, float(np.max(rowmax) - np.max(m_before))))"),
     ("lambda_diagonal_first", "return cands + diags", "return diags + cands"),
     # mean correction
     ("stand_in_without_count", "logits[:, n] = sigma * (q_rows @ kbar) + math.log(c1 - c0)",

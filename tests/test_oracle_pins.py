@@ -102,6 +102,46 @@ def test_lambda_hand_example(case):
     assert kept == expect
 
 
+def _stat(x):
+    return math.inf if x == "inf" else float(x)
+
+
+@pytest.mark.parametrize("case", ["main", "boundary"])
+def test_lambda_decision_statistics_hand_trace(case):
+    """The decision statistic of every candidate, max_r(rowmax_r - m_r) with
+    m_r taken before the block is visited, equals the hand trace (a running
+    max read after the update would give 0 for every kept block)."""
+    g = _load("lambda_vote_example.json")
+    keys = g["keys"] if case == "main" else g["boundary_case"]["keys"]
+    expect = (g["expected_statistics"]["values"] if case == "main"
+              else g["boundary_case"]["expected_statistics"])
+    L = len(keys)
+    q = np.ones((L, 1))
+    k = np.array(keys).reshape(L, 1)
+    got = orc.decision_statistics(q, k, L - 1, 1, 1, 1.0, log_lambda=g["log_lambda"])
+    assert [j for j, _ in got] == list(range(L - 1))
+    assert [x for _, x in got] == [_stat(x) for x in expect]
+
+
+def test_lambda_decision_statistics_two_rows():
+    """Two rows with opposite queries: the statistic is the maximum over rows
+    of each row's own difference, with skips leaving the running max alone."""
+    g = _load("lambda_vote_example.json")["two_rows"]
+    keys = g["keys"]
+    L = len(keys)
+    q = np.array([0.0, 0.0, 0.0, 0.0, 1.0, -1.0]).reshape(L, 1)
+    k = np.array(keys).reshape(L, 1)
+    got = orc.decision_statistics(q, k, 2, 2, 1, 1.0, log_lambda=g["log_lambda"])
+    assert [j for j, _ in got] == [0, 1, 2, 3]
+    assert [x for _, x in got] == [_stat(x) for x in g["expected_statistics"]]
+    r = orc.prefill(q[None], k[None], np.ones((1, L, 1)), Bq=2, Bk=1, sigma=1.0, mode="lambda",
+                    log_lambda=g["log_lambda"])
+    assert [j for j in range(L) if r["keep"][0, 2, j]] == g["expected_kept"]
+    # the keep decision is the statistic against ln(lambda), block by block
+    for j, x in got:
+        assert bool(r["keep"][0, 2, j]) == (x >= g["log_lambda"])
+
+
 @pytest.mark.parametrize("Bq,Bk,L", [(4, 4, 37), (8, 4, 40), (4, 8, 33)])
 def test_lambda_skipped_weights_bounded(Bq, Bk, L):
     """Every post-softmax weight in a skipped block is below lambda."""

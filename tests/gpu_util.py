@@ -97,3 +97,34 @@ def median_table(q64, k64, Bq, Bk, sigma, jitter_seed=0, seq_slices=None):
 
 def default_sigma(d):
     return 1.0 / math.sqrt(d)
+
+
+def guarded_log_lambda(log_lambda, Bq, Bk, sigma, seq_slices):
+    """ln(lambda) moved clear (>= 1e-3) of every lambda decision statistic
+    max_r(rowmax_r - m_r) of every compared query block, computed by the
+    oracle; the same value then goes to the GPU and to the oracle.
+    seq_slices: [(q64 [Hq,L,d], k64 [Hkv,L,d])] per sequence (empty ones
+    allowed)."""
+
+    def stats(ll):
+        out = []
+        for qs, ks in seq_slices:
+            Hq, L = qs.shape[0], qs.shape[1]
+            if L == 0:
+                continue
+            g = Hq // ks.shape[0]
+            for h in range(Hq):
+                for i in range(orc.num_blocks(L, Bq)):
+                    out += [x for _, x in orc.decision_statistics(qs[h], ks[h // g], i, Bq, Bk,
+                                                                   sigma, log_lambda=ll)]
+        return np.asarray(out)
+
+    ll, _ = guard.guard_log_lambda(log_lambda, stats)
+    return ll
+
+
+def varlen_slices(q64, k64, cu):
+    """Per-sequence (q, k) views of packed [H, T, d] arrays."""
+    c = [int(x) for x in cu]
+    return [(q64[:, a:e], k64[:, a:e]) for a, e in zip(c[:-1], c[1:])]
+

@@ -61,14 +61,16 @@ def test_corrected_lambda_gate_varlen_matches_oracle(cuda_device):
     q, cu = wl.pack_varlen(qs)
     k, _ = wl.pack_varlen(ks)
     v, _ = wl.pack_varlen(vs)
+    ll = gu.guarded_log_lambda(-1.0, B, B, gu.default_sigma(d),
+                               gu.varlen_slices(gu.to64(q), gu.to64(k), cu.tolist()))
     r = _bsfa().prefill(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
                         cu_seqlens=cu.to(cuda_device), max_seqlen=max(lens), mode="lambda",
-                        log_lambda=-1.0, mean_correction=True, return_bitmap=True,
+                        log_lambda=ll, mean_correction=True, return_bitmap=True,
                         return_lse=True)
     torch.cuda.synchronize()
     assert _bsfa().api.device_error() == 0
     ref = orc.prefill_varlen(gu.to64(q), gu.to64(k), gu.to64(v), cu.numpy(), Bq=B, Bk=B,
-                             mode="lambda", log_lambda=-1.0, mean_correction=True)
+                             mode="lambda", log_lambda=ll, mean_correction=True)
     bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, lens, B, B)
     assert clean
     for n, Ln in enumerate(lens):
@@ -115,9 +117,10 @@ def test_fp16_corrected_matches_oracle(cuda_device):
     Hq, Hkv, L, d = 2, 2, 600, 64
     x = wl.layer_inputs(Hq, Hkv, L, d, 450, skip_rate=0.5, dtype=torch.float16)
     q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
+    ll = gu.guarded_log_lambda(-1.0, B, B, gu.default_sigma(d), [(q64, k64)])
     r = _run(x.q.to(cuda_device)[None], x.k.to(cuda_device)[None], x.v.to(cuda_device)[None],
-             mode="lambda", log_lambda=-1.0, mean_correction=True)
-    ref = orc.prefill(q64, k64, v64, Bq=B, Bk=B, mode="lambda", log_lambda=-1.0,
+             mode="lambda", log_lambda=ll, mean_correction=True)
+    ref = orc.prefill(q64, k64, v64, Bq=B, Bk=B, mode="lambda", log_lambda=ll,
                       mean_correction=True)
     bits, _ = gu.unpack_bitmap(r["bitmap"], Hq, [L], B, B)
     assert np.array_equal(bits[0], ref["keep"])
@@ -148,3 +151,39 @@ def test_block_mean_pass_head_limit(cuda_device):
     assert e.value.status == 2
     torch.cuda.synchronize()
     assert b.api.device_error() == 0
+
+
+def test_refused_call_writes_nothing(cuda_device):
+    """A call refused for the block-mean pass's head limit (d * Hkv > 1024)
+    returns BSFA_ERR_UNSUPPORTED before anything is launched: the caller's
+    block counters, bitmap, output, LSE and workspace, filled with sentinels,
+    come back untouched.  Called through the C ABI directly."""
+    import ctypes
+
+    from block_sparse_gated_gb300 import _native, api
+    Hq = Hkv = 16
+    L, d = 300, 128
+    x = wl.layer_inputs(Hq, Hkv, L, d, 462, skip_rate=0.5)
+    q, k, v = (t.to(cuda_device)[None] for t in (x.q, x.k, x.v))
+    T = torch.full((Hq, 1), 0.5, device=cuda_device)
+    sent = 0x5A5A5A5A5A5A5A5A
+    counts = torch.full((3,), sent, dtype=torch.int64, device=cuda_device)
+    o = torch.full_like(q, 7.0)
+    bm = torch.full((3, Hq, 1), 0x12345678, dtype=torch.int32, device=cuda_device)
+    lse = torch.full((Hq, L), 3.0, dtype=torch.float32, device=cuda_device)
+    ws = torch.full((1 << 20,), 0xA5, dtype=torch.uint8, device=cuda_device)
+    p = api._params(q, k, v, o, layout=None, cu_seqlens=None, max_seqlen=None, block_q=B,
+                    block_k=B, softmax_scale=None, mode="threshold", thresholds=T,
+                    log_lambda=None, mean_correction=True)
+    p.block_counts, p.kept_bitmap, p.lse = counts.data_ptr(), bm.data_ptr(), lse.data_ptr()
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    torch.cuda.synchronize()
+    status = _native.lib().bsfa_prefill_fwd(ctypes.byref(p), api._stream(None, cuda_device))
+    torch.cuda.synchronize()
+    assert status == 2
+    assert _bsfa().api.device_error() == 0
+    assert torch.all(counts == sent)
+    assert torch.all(o == 7.0)
+    assert torch.all(bm == 0x12345678)
+    assert torch.all(lse == 3.0)
+    assert torch.all(ws == 0xA5)

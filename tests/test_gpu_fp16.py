@@ -15,7 +15,6 @@ import torch
 
 from block_sparse_gated_gb300 import workloads as wl
 from oracle import bsfa_oracle as orc
-from oracle import guard
 from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
@@ -104,17 +103,7 @@ def test_fp16_lambda_gate_matches_oracle(cuda_device, Bq, Bk):
     x, q, k, v = _inputs(Hq, Hkv, L, d, 131, cuda_device, skip_rate=0.5, block=Bk)
     q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
     sigma = gu.default_sigma(d)
-    nq = orc.num_blocks(L, Bq)
-
-    def stats(ll):
-        out = []
-        for h in range(Hq):
-            for i in range(nq):
-                out += [s for _, s in orc.decision_statistics(q64[h], k64[h // (Hq // Hkv)], i,
-                                                              Bq, Bk, sigma, log_lambda=ll)]
-        return np.asarray(out)
-
-    ll, _ = guard.guard_log_lambda(-1.0, stats)
+    ll = gu.guarded_log_lambda(-1.0, Bq, Bk, sigma, [(q64, k64)])
     r = _run(q, k, v, block_q=Bq, block_k=Bk, mode="lambda", log_lambda=ll)
     ref = orc.prefill(q64, k64, v64, Bq=Bq, Bk=Bk, mode="lambda", log_lambda=ll)
     _check(r, ref, Hq, L, Bq, Bk)
@@ -131,12 +120,14 @@ def test_fp16_varlen_lambda_matches_oracle(cuda_device):
     v, _ = wl.pack_varlen([p.v if p else torch.empty(Hkv, 0, d, dtype=F16) for p in parts])
     b = _bsfa()
     dev = cuda_device
+    ll = gu.guarded_log_lambda(-1.0, B, B, gu.default_sigma(d),
+                               gu.varlen_slices(gu.to64(q), gu.to64(k), cu.tolist()))
     r = b.prefill(q.to(dev), k.to(dev), v.to(dev), cu_seqlens=cu.to(dev), max_seqlen=max(lens),
-                  mode="lambda", log_lambda=-1.0, return_bitmap=True, return_lse=True)
+                  mode="lambda", log_lambda=ll, return_bitmap=True, return_lse=True)
     torch.cuda.synchronize()
     assert b.api.device_error() == 0
     ref = orc.prefill_varlen(gu.to64(q), gu.to64(k), gu.to64(v), cu.numpy(), Bq=B, Bk=B,
-                             mode="lambda", log_lambda=-1.0)
+                             mode="lambda", log_lambda=ll)
     bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, lens, B, B)
     assert clean
     for n, Ln in enumerate(lens):

@@ -72,7 +72,8 @@ def test_paged_batched_equals_contiguous(cuda_device, mode, page, kv_layout):
     if mode == "threshold":
         kw["thresholds"] = _median_T(xs, Hq, B, gu.default_sigma(d), cuda_device)
     elif mode == "lambda":
-        kw["log_lambda"] = -1.0
+        kw["log_lambda"] = gu.guarded_log_lambda(
+            -1.0, B, B, gu.default_sigma(d), [(gu.to64(x.q), gu.to64(x.k)) for x in xs])
     b = _bsfa()
     ref = b.prefill(q, k, v, **kw)
     got = b.prefill(q, kpool.to(cuda_device), vpool.to(cuda_device),
@@ -132,7 +133,8 @@ def test_paged_fp16_and_64_blocks_equal_contiguous(cuda_device):
     q, k, v = (t.to(cuda_device)[None] for t in (x.q, x.k, x.v))
     kpool, table = _page_pool([x.k], page, "pthd", seed=3)
     vpool, _ = _page_pool([x.v], page, "pthd", seed=3)
-    kw = dict(mode="lambda", log_lambda=-1.0, block_q=Bs, block_k=Bs, return_bitmap=True,
+    ll = gu.guarded_log_lambda(-1.0, Bs, Bs, gu.default_sigma(d), [(gu.to64(x.q), gu.to64(x.k))])
+    kw = dict(mode="lambda", log_lambda=ll, block_q=Bs, block_k=Bs, return_bitmap=True,
               return_lse=True, return_counts=True)
     b = _bsfa()
     ref = b.prefill(q, k, v, **kw)

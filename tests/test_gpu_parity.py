@@ -13,7 +13,6 @@ import torch
 
 from block_sparse_gated_gb300 import workloads as wl
 from oracle import bsfa_oracle as orc
-from oracle import guard
 from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
@@ -136,17 +135,7 @@ def test_lambda_gate_matches_oracle(cuda_device, Bq, Bk, skip_rate):
     x, q, k, v = _inputs(Hq, Hkv, L, d, 31, cuda_device, skip_rate=skip_rate, block=Bk)
     q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
     sigma = gu.default_sigma(d)
-    nq = orc.num_blocks(L, Bq)
-
-    def stats(ll):
-        out = []
-        for h in range(Hq):
-            for i in range(nq):
-                out += [s for _, s in orc.decision_statistics(q64[h], k64[h // (Hq // Hkv)], i,
-                                                              Bq, Bk, sigma, log_lambda=ll)]
-        return np.asarray(out)
-
-    ll, _ = guard.guard_log_lambda(-1.0 if skip_rate > 0 else -1e30, stats)
+    ll = gu.guarded_log_lambda(-1.0 if skip_rate > 0 else -1e30, Bq, Bk, sigma, [(q64, k64)])
     r = _run(q, k, v, block_q=Bq, block_k=Bk, mode="lambda", log_lambda=ll)
     ref = orc.prefill(q64, k64, v64, Bq=Bq, Bk=Bk, mode="lambda", log_lambda=ll)
     bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, [L], Bq, Bk)
@@ -185,7 +174,8 @@ def test_varlen_matches_oracle(cuda_device, mode):
         T, _, _ = gu.guarded_thresholds(None, None, T, B, B, sigma, seq_slices=slices)
         kw = dict(thresholds=torch.from_numpy(T).to(cuda_device))
     elif mode == "lambda":
-        kw = dict(log_lambda=-1.0)
+        ll = gu.guarded_log_lambda(-1.0, B, B, sigma, gu.varlen_slices(q64, k64, cu.tolist()))
+        kw = dict(log_lambda=ll)
     b = _bsfa()
     r = b.prefill(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
                   cu_seqlens=cu.to(cuda_device), max_seqlen=max(lens), mode=mode,
@@ -196,7 +186,7 @@ def test_varlen_matches_oracle(cuda_device, mode):
     if mode == "threshold":
         okw["thresholds"] = T.astype(np.float64)
     if mode == "lambda":
-        okw["log_lambda"] = -1.0
+        okw["log_lambda"] = ll
     ref = orc.prefill_varlen(q64, k64, v64, cu.numpy(), Bq=B, Bk=B, **okw)
     bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, lens, B, B)
     assert clean

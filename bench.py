@@ -34,7 +34,14 @@ METRIC = ("prefill attention ms/layer & effective TFLOPS (frac of bf16 peak) at 
 UNIT = "TFLOP/s (effective)"
 
 
-def code_digest(paths):
+# The attention kernel's own sources: an ncu record stays valid while these
+# are unchanged (host-side code, such as argument checks, does not affect it).
+KERNEL_SOURCES = ["block_sparse_gated_gb300/csrc/bsfa_fwd.cuh",
+                  "block_sparse_gated_gb300/csrc/ptx.cuh",
+                  "block_sparse_gated_gb300/csrc/inst_fwd.cuh"]
+
+
+def code_digest(paths=KERNEL_SOURCES):
     """sha256 of the given sources with C/C++ comments and all whitespace
     removed: it changes when the code changes, not when a comment does."""
     import hashlib
@@ -54,7 +61,7 @@ def _recorded_traffic(workload):
     path = os.path.join(ROOT, "profiles", f"bsfa_fwd_kernel_dram_{workload}.json")
     try:
         rec = json.load(open(path))
-        if code_digest(rec["sources"]) != rec["code_sha256"]:
+        if rec["sources"] != KERNEL_SOURCES or code_digest() != rec["code_sha256"]:
             return None
         return float(rec["mean_bytes_per_launch"])
     except Exception:
@@ -68,7 +75,7 @@ def _recorded_ncu(workload="llama8b-L32768"):
     path = os.path.join(ROOT, "profiles", f"bsfa_fwd_kernel_full_{workload}.json")
     try:
         rec = json.load(open(path))
-        if code_digest(rec["sources"]) != rec["code_sha256"]:
+        if rec["sources"] != KERNEL_SOURCES or code_digest() != rec["code_sha256"]:
             return None
         return {"workload": rec["workload"], "kernel": rec["kernel"],
                 "tensor_pipe_active_pct": rec["tensor_pipe_active_pct_of_elapsed"],
@@ -208,6 +215,22 @@ def aggregate_step(ms_step, step_flops, world, device=None):
     return ms_step, world * step_flops / (ms_step * 1e-3) / 1e12
 
 
+def aggregate_shards(ms_step, step_flops, world, device=None):
+    """Whole-job figures of a head-sharded run: each rank computes its own KV
+    heads (and their query heads) of the same layer, the step time is the
+    maximum over ranks, and the value is the FLOPs summed over ranks over
+    that time (TFLOP/s).  Returns (ms, value, total FLOPs)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(ms_step)], dtype=torch.float64, device=device)
+        f = torch.tensor([float(step_flops)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+        ms_step, step_flops = float(t.item()), float(f.item())
+    return ms_step, step_flops / (ms_step * 1e-3) / 1e12, step_flops
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -220,6 +243,12 @@ def run_ours(args, rank, world, local_rank):
     cfg = W["cfg"]
     Hq, d, Bq, Bk, L = cfg["Hq"], cfg["d"], cfg["Bq"], cfg["Bk"], cfg["L"]
     q, k, v, T = W["q"][None], W["k"][None], W["v"][None], W["T"]
+    sharded = args.shard == "heads"
+    if sharded:
+        from block_sparse_gated_gb300.shard import head_shard, shard_tensors
+        sh = head_shard(Hq, cfg["Hkv"], rank, world)
+        q, k, v, T = (t.contiguous() for t in shard_tensors(sh, q, k, v, T))
+        Hq = sh.num_heads_q
     ks = cfg["ks"]
     slices = [T[i].contiguous() for i in range(len(ks))]
     outs = [torch.empty_like(q) for _ in ks]
@@ -264,7 +293,10 @@ def run_ours(args, rank, world, local_rank):
     clocks = clk.summary()
     total_ms = t_start.elapsed_time(t_end)
     step_flops = sum(flops)
-    ms_step, value = aggregate_step(total_ms / args.steps, step_flops, world, dev)
+    if sharded:
+        ms_step, value, _ = aggregate_shards(total_ms / args.steps, step_flops, world, dev)
+    else:
+        ms_step, value = aggregate_step(total_ms / args.steps, step_flops, world, dev)
     per_slice_ms = [statistics.mean(starts[s][i].elapsed_time(ends[s][i]) for s in range(args.steps))
                     for i in range(len(ks))]
     launch_achieved = sum(flops) / (sum(per_slice_ms) * 1e-3) / 1e12
@@ -283,14 +315,17 @@ def run_ours(args, rank, world, local_rank):
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "strong" if sharded else "weak",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; Llama-3.1-8B attention shapes; no dataset)",
         "config": {"workload": args.workload, "Hq": Hq, "Hkv": cfg["Hkv"], "d": d, "L": L,
                    "Bq": Bq, "Bk": Bk, "budgets_k": ks, "calibration": f"{cfg['n_cal']} x "
                    f"{cfg['cal_L']} tokens",
                    "l2": f"inputs larger than L2 (Q {q.numel() * 2 / 2**20:.0f} MiB, K and V "
                          f"{k.numel() * 2 / 2**20:.0f} MiB each); no flush",
-                   "parallelism": f"replica x{world}"},
+                   "parallelism": (f"heads x{world} (rank 0: KV heads "
+                                   f"{sh.kv_heads.start}-{sh.kv_heads.stop - 1}, slices below are "
+                                   f"rank 0's)" if sharded else f"replica x{world}")},
         "slices": slices_out,
         "roofline": {"bound": "tensor", "achieved": round(launch_achieved, 1),
                      "peak": peak_sust, "unit": "TFLOP/s",
@@ -306,15 +341,15 @@ def run_ours(args, rank, world, local_rank):
                       "tflops_qk": round(W["cal_tflops"], 1)},
     }
 
-    if not args.no_sweep and rank == 0:
+    if not args.no_sweep and rank == 0 and not sharded:
         result["paged_kv"] = paged_leg(q, k, v, slices, ks, outs, Bq, Bk, dev)
         result["mean_correction"] = mean_correction_leg(q, k, v, slices, ks, Bq, Bk, dev)
         result["lambda_sweep"] = lambda_sweep(dev, args)
         result["llama8b_L32768"] = llama_32k_leg(dev)
         result["varlen_8seq_32layer"] = varlen_32layer_leg(dev)
-    if not args.no_e2e:
+    if not args.no_e2e and not sharded:
         result["e2e"] = e2e(q, k, v, slices, flops, Bq, Bk, args, dev)
-    if not args.no_cpu and rank == 0 and world == 1:
+    if not args.no_cpu and rank == 0 and world == 1 and not sharded:
         result["cpu_baseline"] = cpu_baseline(args.workload, W, cnts)
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -754,6 +789,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--shard", default="replica", choices=["replica", "heads"],
+                    help="replica: every rank runs the whole layer (weak scaling); heads: "
+                         "the KV-head groups of the layer are split over the ranks (strong)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

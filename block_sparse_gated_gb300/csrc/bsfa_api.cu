@@ -359,6 +359,8 @@ static bsfa_status validate(const bsfa_fwd_params* p) {
         p->block_table != nullptr || (p->flags & BSFA_FLAG_V_ALWAYS) ||
         (max_len_of(p) + TILE - 1) / TILE > 32 * CORR_WORDS)
       return BSFA_ERR_UNSUPPORTED;
+    // The block-mean pass runs one thread per (element, KV head) in one CTA.
+    if (p->head_dim * p->num_heads_kv > 1024) return BSFA_ERR_UNSUPPORTED;
   }
   if (p->batch == 0 || p->seqlen == 0) return BSFA_OK;
   if (!p->q || !p->k || !p->v || !p->o) return BSFA_ERR_INVALID_ARG;
@@ -520,8 +522,7 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
                                                        p->block_counts);
   if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;
   if (corr) {
-    const dim3 mb_block(d, p->num_heads_kv);
-    if (d * p->num_heads_kv > 1024) return BSFA_ERR_UNSUPPORTED;
+    const dim3 mb_block(d, p->num_heads_kv);  // d * Hkv <= 1024, checked by validate()
     const auto* kk = static_cast<const uint16_t*>(p->k);
     const auto* vv = static_cast<const uint16_t*>(p->v);
     const long long ksb = varlen ? 0 : p->k_stride[0], vsb = varlen ? 0 : p->v_stride[0];
@@ -602,9 +603,6 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
   dp.err = error_word();
   if (dp.err == nullptr) return BSFA_ERR_CUDA;
 
-  prep_kernel<<<1, PREP_THREADS, sizeof(int) * (1 + (size_t)max_tiles), stream>>>(
-      nullptr, 1, L, 0, Bq, max_tiles, cv.seqinfo, cv.tiles, cv.ntot, nullptr);
-  if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return BSFA_ERR_CUDA;
   const long long units = (long long)max_tiles * Hkv * (g / nq);
@@ -630,7 +628,11 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
                            (int)sel_smem) != cudaSuccess)
     return BSFA_ERR_CUDA;
   const int sel_threads = sort_n < 1024 ? (sort_n < 32 ? 32 : sort_n) : 1024;
-  if (sel_threads < n_k) return BSFA_ERR_UNSUPPORTED;
+  if (sel_threads < n_k) return BSFA_ERR_UNSUPPORTED;  // never: n_k <= 16 < 32
+
+  prep_kernel<<<1, PREP_THREADS, sizeof(int) * (1 + (size_t)max_tiles), stream>>>(
+      nullptr, 1, L, 0, Bq, max_tiles, cv.seqinfo, cv.tiles, cv.ntot, nullptr);
+  if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;
 
   for (int n = 0; n < n_samples; ++n) {
     Maps m;

@@ -30,10 +30,9 @@
  *   - Calls are asynchronous on `stream` and never synchronise the host,
  *     except bsfa_device_error which synchronises `stream` by design.
  *   - Errors that the host can detect are returned before anything is
- *     launched, with one exception: the mean-correction head limit
- *     (BSFA_FLAG_MEAN_CORRECTION) is returned after the scheduling pre-pass
- *     has been queued, which writes only the workspace.  A device-side wait that ran out of time (a hang guard, never
- *     expected in a correct run) sets a device error word; it is reported by
+ *     launched: a rejected call writes no memory the caller can see.  A
+ *     device-side wait that ran out of time (a hang guard, never expected in
+ *     a correct run) sets a device error word; it is reported by
  *     bsfa_device_error.
  *   - No C++ exception crosses this boundary.
  *   - Size limits (BSFA_ERR_UNSUPPORTED beyond them): at most 4096 sequences
@@ -106,9 +105,8 @@ typedef enum {
    * them).  Requires block_q == block_k == 128, contiguous K/V (block_table
    * NULL), no BSFA_FLAG_V_ALWAYS, sequences of at most 524288 tokens and
    * head_dim * num_heads_kv <= 1024 (one thread per element in the block-mean
-   * pass: Hkv <= 8 at d = 128, <= 16 at d = 64); else BSFA_ERR_UNSUPPORTED.
-   * The last limit is checked after the scheduling pre-pass has been queued
-   * on the stream (it only writes the workspace). */
+   * pass: Hkv <= 8 at d = 128, <= 16 at d = 64); else BSFA_ERR_UNSUPPORTED,
+   * returned before anything is launched. */
   BSFA_FLAG_MEAN_CORRECTION = 2
 } bsfa_flag;
 
@@ -207,8 +205,7 @@ bsfa_status bsfa_bitmap_words_per_row(const bsfa_fwd_params* p, int* words_per_r
 /* Gated causal prefill.  Validates `p`, then enqueues on `stream` a small
  * scheduling kernel, the block-mean kernel when BSFA_FLAG_MEAN_CORRECTION is
  * set, and the persistent attention kernel.  Asynchronous.
- * Errors: BSFA_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE before any launch
- * (except the mean-correction head limit, see BSFA_FLAG_MEAN_CORRECTION);
+ * Errors: BSFA_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE before any launch;
  * BSFA_ERR_CUDA if a launch or descriptor encode fails. */
 bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream);
 

@@ -162,6 +162,18 @@ def test_mean_correction_parameters_are_validated_on_the_host(libpath):
     p.flags = _native.FLAG_MEAN_CORRECTION
     p.block_table, p.block_table_stride, p.page_size, p.num_pages = 1 << 12, 8, 128, 8
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # contiguous K/V only
+    # The block-mean pass's head limit (d * Hkv <= 1024) is part of the
+    # validation too: it is refused here, with no workspace and no device.
+    p.block_table, p.block_table_stride, p.page_size, p.num_pages = None, 0, 0, 0
+    p.num_heads_q, p.num_heads_kv = 16, 16
+    p.q_stride[:] = p.o_stride[:] = (16 * 1000 * 128, 1000 * 128, 128)
+    p.k_stride[:] = p.v_stride[:] = (16 * 1000 * 128, 1000 * 128, 128)
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2
+    p.thresholds, p.thresholds_nq = 1 << 20, 1
+    p.head_dim = 64  # 16 x 64 = 1024: within the limit, so only the workspace is missing
+    p.q_stride[:] = p.o_stride[:] = (16 * 1000 * 64, 1000 * 64, 64)
+    p.k_stride[:] = p.v_stride[:] = (16 * 1000 * 64, 1000 * 64, 64)
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 5
 
 
 def test_size_limits_are_rejected_on_the_host(libpath):

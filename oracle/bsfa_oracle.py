@@ -216,6 +216,101 @@ def decision_statistics(q_h, k_h, i, Bq, Bk, sigma, log_lambda=NEG_INF):
 
 
 # ---------------------------------------------------------------------------
+# Whole-head forms of the two gates, for comparing every block of a long
+# sequence: the same definitions as above, one query block at a time.
+# ---------------------------------------------------------------------------
+def _as_torch64(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64))
+
+
+def _key_major_scores(qt, kt, r0, r1, nkeys, sigma):
+    """sigma * K[:nkeys] Q[r0:r1]^T in fp64 ([keys, rows]) from torch fp64
+    copies of one head's queries and keys: the scores of the query rows
+    against the first nkeys keys, with the keys as rows (each key block is
+    then one contiguous run of Bk rows).  torch's CPU matmul is the library
+    product (multithreaded)."""
+    return (kt[:nkeys] @ qt[r0:r1].T) * sigma
+
+
+def block_maxima(q_h, k_h, Bq, Bk, sigma) -> np.ndarray:
+    """s_max(i, j) of every candidate pair of one head ("Exact-Score Gating":
+    the maximum over the whole Bq x Bk tile of the scaled scores), as an
+    [nq, nk] float64 array with NaN where j is not a candidate of i.
+
+    A candidate's keys all precede every row of its query block, so its tile
+    needs no causal mask: for query block i the scores of its rows against
+    the keys of its candidates (key blocks 0 .. ncand-1) are one product,
+    and each candidate's maximum is taken over its Bk keys and all rows."""
+    import torch
+    L = q_h.shape[0]
+    nq, nk = num_blocks(L, Bq), num_blocks(L, Bk)
+    out = np.full((nq, nk), np.nan)
+    qt, kt = _as_torch64(q_h), _as_torch64(k_h)
+    for i in range(nq):
+        r0, r1 = i * Bq, min((i + 1) * Bq, L)
+        ncand = (i * Bq) // Bk  # key blocks j with (j + 1) * Bk <= i * Bq
+        if ncand == 0:
+            continue
+        sT = _key_major_scores(qt, kt, r0, r1, ncand * Bk, sigma)
+        out[i, :ncand] = torch.amax(sT.reshape(ncand, Bk * (r1 - r0)), dim=1).numpy()
+    return out
+
+
+def keep_threshold_all(smax: np.ndarray, T_h, L: int, Bq: int, Bk: int) -> np.ndarray:
+    """Threshold keep matrix [nq, nk] of one head from its block maxima
+    (``block_maxima``) and its threshold row T_h (length nT, looked up at
+    min(i, nT - 1)): candidates kept iff s_max >= T, the diagonal region
+    always kept, invisible blocks False."""
+    nq, nk = smax.shape
+    keep = np.zeros((nq, nk), dtype=bool)
+    for i in range(nq):
+        t = float(T_h[threshold_index(i, len(T_h))])
+        for j in range(min(nk, num_blocks(min((i + 1) * Bq, L), Bk))):  # j past these: invisible
+            cls = block_class(i, j, Bq, Bk, L)
+            if cls == CANDIDATE:
+                keep[i, j] = smax[i, j] >= t
+            elif cls == DIAGONAL:
+                keep[i, j] = True
+    return keep
+
+
+def lambda_all(q_h, k_h, Bq, Bk, sigma, log_lambda):
+    """lambda gate ("Vote, then skip") over every query block of one head:
+    returns (keep [nq, nk] bool, statistic [nq, nk] float64 with NaN off the
+    candidates).  Per query block the candidates are visited in ascending
+    key order, each row keeping its exact running max over kept blocks
+    (from -inf); block j's statistic is max_r(rowmax_r - m_r) before the
+    visit, and it is kept iff that is >= ln(lambda).  The diagonal region is
+    kept; its scores never reach a decision, since it is visited last."""
+    import torch
+    L = q_h.shape[0]
+    nq, nk = num_blocks(L, Bq), num_blocks(L, Bk)
+    keep = np.zeros((nq, nk), dtype=bool)
+    stat = np.full((nq, nk), np.nan)
+    qt, kt = _as_torch64(q_h), _as_torch64(k_h)
+    for i in range(nq):
+        r0, r1 = i * Bq, min((i + 1) * Bq, L)
+        ncand = (i * Bq) // Bk
+        for j in range(ncand, min(nk, num_blocks(r1, Bk))):  # the diagonal region
+            if block_class(i, j, Bq, Bk, L) == DIAGONAL:
+                keep[i, j] = True
+        if ncand == 0:
+            continue
+        sT = _key_major_scores(qt, kt, r0, r1, ncand * Bk, sigma)
+        rowmax = torch.amax(sT.reshape(ncand, Bk, r1 - r0), dim=1).numpy()  # [candidate, row]
+        m = np.full(r1 - r0, NEG_INF)
+        for j in range(ncand):
+            with np.errstate(invalid="ignore"):
+                st = float(np.max(rowmax[j] - m))  # +inf while m is -inf
+            stat[i, j] = st
+            if st >= log_lambda:
+                keep[i, j] = True
+                m = np.maximum(m, rowmax[j])
+    return keep, stat
+
+
+# ---------------------------------------------------------------------------
 # Renormalised attention over the kept keys ("Selective Streaming
 # Aggregation": a skipped block is absent from numerator and denominator).
 # ---------------------------------------------------------------------------

@@ -76,6 +76,9 @@ MUTANTS = [
     ("lambda_tile_max_statistic", "rowmax = np.max(s[:, j * Bk:(j + 1) * Bk], axis=1)",
      "rowmax = np.full(s.shape[0], np.max(s[:, j * Bk:(j + 1) * Bk]))"),
     ("lambda_descending", "return cands + diags", "return cands[::-1] + diags"),
+    ("lambda_max_raised_by_skipped_block",
+     "        keep[j] = kept\n        if kept:\n            m = np.maximum(m, rowmax)",
+     "        keep[j] = kept\n        m = np.maximum(m, rowmax)"),
     ("lambda_statistic_after_update",
      "        if trace is not None:\n            trace.append((j, m.copy(), rowmax.copy(), kept))\n"
      "        keep[j] = kept\n        if kept:\n            m = np.maximum(m, rowmax)",
@@ -86,6 +89,19 @@ MUTANTS = [
     ("lambda_statistic_tile_wide", "out.append((j, float(np.max(rowmax - m_before))))",
      "out.append((j, float(np.max(rowmax) - np.max(m_before))))"),
     ("lambda_diagonal_first", "return cands + diags", "return diags + cands"),
+    # whole-head forms
+    ("block_maxima_partial_candidates", "        ncand = (i * Bq) // Bk  # key blocks j with",
+     "        ncand = (i * Bq + Bk - 1) // Bk  # key blocks j with"),
+    ("block_maxima_first_row",
+     "out[i, :ncand] = torch.amax(sT.reshape(ncand, Bk * (r1 - r0)), dim=1).numpy()",
+     "out[i, :ncand] = torch.amax(sT.reshape(ncand, Bk, r1 - r0), dim=1)[:, 0].numpy()"),
+    ("whole_head_threshold_gt", "keep[i, j] = smax[i, j] >= t", "keep[i, j] = smax[i, j] > t"),
+    ("whole_head_diagonal_gated", "            elif cls == DIAGONAL:\n                keep[i, j] = True",
+     "            elif cls == DIAGONAL:\n                keep[i, j] = smax[i, j] >= t"),
+    ("whole_head_lambda_gt", "            if st >= log_lambda:", "            if st > log_lambda:"),
+    ("whole_head_lambda_max_on_skip",
+     "                keep[i, j] = True\n                m = np.maximum(m, rowmax[j])",
+     "                keep[i, j] = True\n            m = np.maximum(m, rowmax[j])"),
     # mean correction
     ("stand_in_without_count", "logits[:, n] = sigma * (q_rows @ kbar) + math.log(c1 - c0)",
      "logits[:, n] = sigma * (q_rows @ kbar)"),

@@ -162,10 +162,11 @@ def test_llama_128k_k128_mean_correction_full_size(cuda_device):
     assert 0.5 < skip < 1.0
 
 
-@pytest.mark.parametrize("k_index", [1, 2])
+@pytest.mark.parametrize("k_index", [0, 1, 2])
 def test_llama_128k_full_size(cuda_device, k_index):
-    """k = 128 gates; k = 512 has no table entry with 512 candidates at the
-    64K calibration length, so every entry is -inf and nothing is skipped."""
+    """k = 32 and k = 128 gate; k = 512 has no table entry with 512
+    candidates at the 64K calibration length, so every entry is -inf and
+    nothing is skipped."""
     worst, skip = _threshold_case(cuda_device, "llama8b-L131072", k_index)
     if k_index == 2:
         assert skip == 0.0
@@ -173,7 +174,7 @@ def test_llama_128k_full_size(cuda_device, k_index):
         assert skip > 0.0
 
 
-@pytest.mark.parametrize("rate", [0.5, 0.9])
+@pytest.mark.parametrize("rate", [0.25, 0.5, 0.75, 0.9])
 def test_lambda_sweep_64k_full_size(cuda_device, rate):
     cfg = wl.WORKLOADS["lambda-sweep-L65536"]
     Hq, Hkv, d, B, L = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["Bk"], cfg["L"]

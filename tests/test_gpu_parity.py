@@ -129,7 +129,8 @@ def test_tiny_workload_calibrated(cuda_device):
 
 
 # ---------------------------------------------------------------- lambda gate
-@pytest.mark.parametrize("Bq,Bk,skip_rate", [(128, 128, 0.5), (64, 64, 0.5), (128, 128, 0.0)])
+@pytest.mark.parametrize("Bq,Bk,skip_rate", [(128, 128, 0.5), (64, 64, 0.5), (128, 64, 0.5),
+                                             (64, 128, 0.5), (128, 128, 0.0)])
 def test_lambda_gate_matches_oracle(cuda_device, Bq, Bk, skip_rate):
     Hq, Hkv, L, d = 4, 2, 1500, 128
     x, q, k, v = _inputs(Hq, Hkv, L, d, 31, cuda_device, skip_rate=skip_rate, block=Bk)

@@ -106,6 +106,20 @@ def _stat(x):
     return math.inf if x == "inf" else float(x)
 
 
+def test_lambda_skipped_block_never_raises_the_running_max():
+    """With ln(lambda) > 0 a skipped block can lie above the running max; it
+    must still leave it alone (hand trace)."""
+    g = _load("lambda_vote_example.json")["positive_log_lambda"]
+    keys = g["keys"]
+    L = len(keys)
+    q, k = np.ones((L, 1)), np.array(keys).reshape(L, 1)
+    got = orc.decision_statistics(q, k, L - 1, 1, 1, 1.0, log_lambda=g["log_lambda"])
+    assert [x for _, x in got] == [_stat(x) for x in g["expected_statistics"]]
+    r = orc.prefill(q[None], k[None], np.ones((1, L, 1)), Bq=1, Bk=1, sigma=1.0, mode="lambda",
+                    log_lambda=g["log_lambda"])
+    assert [j for j in range(L) if r["keep"][0, L - 1, j]] == g["expected_kept"]
+
+
 @pytest.mark.parametrize("case", ["main", "boundary"])
 def test_lambda_decision_statistics_hand_trace(case):
     """The decision statistic of every candidate, max_r(rowmax_r - m_r) with
@@ -537,3 +551,106 @@ def test_mean_correction_without_skips_changes_nothing():
     lam = orc.prefill(q, k, v, Bq=16, Bk=16, mode="lambda", log_lambda=-np.inf,
                       mean_correction=True)
     assert np.array_equal(lam["out"], a["out"])
+
+
+# ---------------------------------------------------------------------------
+# Whole-head forms used for full-size bitmap comparisons
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("Bq,Bk,L", [(4, 4, 37), (8, 4, 41), (4, 8, 35), (3, 2, 17)])
+def test_block_maxima_brute_force(Bq, Bk, L):
+    """Every candidate's s_max from explicit loops over its rows and keys
+    (dot products one by one); NaN exactly where j is not a candidate."""
+    d, sigma = 3, 0.6
+    q, k = _rand((L, d), 90 + L), _rand((L, d), 91 + L)
+    got = orc.block_maxima(q, k, Bq, Bk, sigma)
+    nq, nk = -(-L // Bq), -(-L // Bk)
+    assert got.shape == (nq, nk)
+    for i in range(nq):
+        rows = range(i * Bq, min((i + 1) * Bq, L))
+        for j in range(nk):
+            keys = range(j * Bk, min((j + 1) * Bk, L))
+            if (j + 1) * Bk <= i * Bq:  # every key precedes every row
+                best = max(sigma * sum(q[r, t] * k[c, t] for t in range(d))
+                           for r in rows for c in keys)
+                assert abs(got[i, j] - best) < 1e-12
+            else:
+                assert np.isnan(got[i, j])
+
+
+@pytest.mark.parametrize("Bq,Bk,L", [(4, 4, 37), (8, 4, 40), (4, 8, 33)])
+def test_whole_head_threshold_gate_equals_per_block_gate(Bq, Bk, L):
+    Hq, Hkv, d = 2, 1, 8
+    q, k, v = _rand((Hq, L, d), 93), _rand((Hkv, L, d), 94), _rand((Hkv, L, d), 95)
+    sigma = 1 / math.sqrt(d)
+    T = _rand((Hq, 3), 96) * 0.4 + 0.6  # three entries: reuse past the table's end
+    r = orc.prefill(q, k, v, Bq=Bq, Bk=Bk, sigma=sigma, thresholds=T)
+    for h in range(Hq):
+        got = orc.keep_threshold_all(orc.block_maxima(q[h], k[0], Bq, Bk, sigma), T[h], L, Bq, Bk)
+        assert np.array_equal(got, r["keep"][h])
+    assert (~r["keep"] & r["candidate"]).any() and (r["keep"] & r["candidate"]).any()
+
+
+def test_whole_head_gates_on_the_worked_example():
+    g = _load("worked_example.json")
+    q, k, _ = _worked_inputs(g["candidate_block_maxima"])
+    L = q.shape[1]
+    smax = orc.block_maxima(q[0], k[0], 1, 1, 1.0)
+    T = np.full(L, -np.inf)
+    T[L - 1] = g["threshold"]
+    keep = orc.keep_threshold_all(smax, T, L, 1, 1)
+    cand = g["candidate_block_maxima"]
+    assert sorted(cand[j] for j in range(len(cand)) if keep[L - 1, j]) == \
+        sorted(g["expected_kept_maxima"])
+    assert keep[L - 1, L - 1]
+    # a maximum equal to the threshold is kept (">=")
+    T[L - 1] = 4.0
+    keep = orc.keep_threshold_all(smax, T, L, 1, 1)
+    assert sorted(cand[j] for j in range(len(cand)) if keep[L - 1, j]) == [4.0, 5.0]
+
+
+@pytest.mark.parametrize("case", ["main", "boundary", "two_rows", "positive_log_lambda"])
+def test_whole_head_lambda_on_the_hand_traces(case):
+    g = _load("lambda_vote_example.json")
+    if case == "positive_log_lambda":
+        c = g[case]
+        keys, ll, Bq = c["keys"], c["log_lambda"], 1
+        q = np.ones((len(keys), 1))
+        i = len(keys) - 1
+        stats, kept = c["expected_statistics"], c["expected_kept"]
+    elif case == "two_rows":
+        c = g["two_rows"]
+        keys, ll, i, Bq = c["keys"], c["log_lambda"], 2, 2
+        q = np.array([0.0, 0.0, 0.0, 0.0, 1.0, -1.0]).reshape(-1, 1)
+        stats, kept = c["expected_statistics"], c["expected_kept"]
+    else:
+        keys = g["keys"] if case == "main" else g["boundary_case"]["keys"]
+        ll, Bq = g["log_lambda"], 1
+        q = np.ones((len(keys), 1))
+        i = len(keys) - 1
+        stats = (g["expected_statistics"]["values"] if case == "main"
+                 else g["boundary_case"]["expected_statistics"])
+        kept = g["expected_kept"] if case == "main" else g["boundary_case"]["expected_kept"]
+    k = np.array(keys).reshape(-1, 1)
+    keep, st = orc.lambda_all(q, k, Bq, 1, 1.0, ll)
+    assert [x for x in st[i] if not np.isnan(x)] == [_stat(x) for x in stats]
+    assert [j for j in range(len(keys)) if keep[i, j]] == kept
+
+
+@pytest.mark.parametrize("Bq,Bk,L", [(4, 4, 37), (8, 4, 40), (4, 8, 33)])
+def test_whole_head_lambda_equals_per_block_gate(Bq, Bk, L):
+    Hq, Hkv, d = 2, 1, 8
+    q, k, v = _rand((Hq, L, d), 97), _rand((Hkv, L, d), 98), _rand((Hkv, L, d), 99)
+    for j in range(1, orc.num_blocks(L, Bk), 2):
+        k[:, j * Bk:(j + 1) * Bk] *= 0.05
+    q *= 2.0
+    sigma, ll = 1 / math.sqrt(d), -0.4
+    r = orc.prefill(q, k, v, Bq=Bq, Bk=Bk, sigma=sigma, mode="lambda", log_lambda=ll)
+    for h in range(Hq):
+        keep, st = orc.lambda_all(q[h], k[0], Bq, Bk, sigma, ll)
+        assert np.array_equal(keep, r["keep"][h])
+        for i in range(orc.num_blocks(L, Bq)):
+            ref = orc.decision_statistics(q[h], k[0], i, Bq, Bk, sigma, log_lambda=ll)
+            assert [j for j, _ in ref] == [j for j in range(st.shape[1]) if not np.isnan(st[i, j])]
+            for j, x in ref:
+                assert st[i, j] == x or abs(st[i, j] - x) < 1e-12
+    assert (~r["keep"] & r["visible"]).any()

@@ -532,13 +532,21 @@ def lambda_sweep(dev, args):
                                          (ms * 1e-3) / 1e12, 1),
                "ms_v_always": round(timed(lambda: bsfa.prefill(
                    q, k, v, mode="lambda", log_lambda=ll, out=out, workspace=ws,
-                   v_always=True)), 3)}
+                   v_always=True)), 3),
+               "ms_pipelined": round(timed(lambda: bsfa.prefill(
+                   q, k, v, mode="lambda", log_lambda=ll, out=out, workspace=ws,
+                   schedule="pipelined")), 3)}
         if r == 0:
             thr = torch.full((Hq, 1), -math.inf, device=dev)
             row["ms_threshold_minus_inf"] = round(timed(lambda: bsfa.prefill(
                 q, k, v, mode="threshold", thresholds=thr, out=out, workspace=ws)), 3)
             row["ms_gate_compiled_out"] = round(timed(lambda: bsfa.prefill(
                 q, k, v, mode="none", out=out, workspace=ws)), 3)
+            row["ms_threshold_minus_inf_pipelined"] = round(timed(lambda: bsfa.prefill(
+                q, k, v, mode="threshold", thresholds=thr, out=out, workspace=ws,
+                schedule="pipelined")), 3)
+            row["ms_gate_compiled_out_pipelined"] = round(timed(lambda: bsfa.prefill(
+                q, k, v, mode="none", out=out, workspace=ws, schedule="pipelined")), 3)
         rows.append(row)
         del x, q, k, v, out
     base = rows[0]["ms_gate_compiled_out"]
@@ -547,7 +555,10 @@ def lambda_sweep(dev, args):
             "zero_skip_overhead_lambda": round(rows[0]["ms"] / base - 1, 4),
             "zero_skip_overhead_threshold": round(rows[0]["ms_threshold_minus_inf"] / base - 1, 4),
             "monotonic": all(a > b for a, b in zip(times, times[1:])),
-            "v_always_over_gated_v": [round(r_["ms_v_always"] / r_["ms"], 4) for r_ in rows]}
+            "v_always_over_gated_v": [round(r_["ms_v_always"] / r_["ms"], 4) for r_ in rows],
+            "pipelined_over_paired": [round(r_["ms_pipelined"] / r_["ms"], 4) for r_ in rows],
+            "schedules": "ms*: paired schedule (two query heads of a GQA group per CTA); "
+                         "*_pipelined: one query head per CTA, next Q.K^T issued ahead of P.V"}
 
 
 def _timed(fn, reps):

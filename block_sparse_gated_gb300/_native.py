@@ -41,6 +41,7 @@ DTYPE_BF16, DTYPE_F16 = 0, 1
 # bsfa_flag
 FLAG_V_ALWAYS = 1
 FLAG_MEAN_CORRECTION = 2
+FLAG_PIPELINED = 4
 
 
 # Every exported symbol and its C signature: (name, restype, argtypes).

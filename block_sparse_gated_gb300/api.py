@@ -110,7 +110,7 @@ def _pool_strides(t: torch.Tensor, kv_layout: str):
 
 def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, softmax_scale,
             mode, thresholds, log_lambda, v_always=False, block_table=None, kv_layout="pthd",
-            mean_correction=False):
+            mean_correction=False, schedule="paired"):
     varlen = cu_seqlens is not None
     if layout is None:
         layout = "htd" if varlen else "bhld"
@@ -176,8 +176,11 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
         p.thresholds, p.thresholds_nq = None, 0
     p.log_lambda = float(log_lambda) if log_lambda is not None else 0.0
     p.dtype = _dtype_code(q)
+    if schedule not in ("paired", "pipelined"):
+        raise ValueError(f"unknown schedule {schedule!r}")
     p.flags = (_native.FLAG_V_ALWAYS if v_always else 0) | \
-        (_native.FLAG_MEAN_CORRECTION if mean_correction else 0)
+        (_native.FLAG_MEAN_CORRECTION if mean_correction else 0) | \
+        (_native.FLAG_PIPELINED if schedule == "pipelined" else 0)
     if paged:
         p.block_table = block_table.data_ptr()
         p.block_table_stride = block_table.stride(0)
@@ -199,7 +202,7 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
             thresholds=None, log_lambda=None, cu_seqlens=None, max_seqlen=None, layout=None,
             out=None, return_bitmap=False, return_lse=False, return_counts=False,
             workspace=None, stream=None, v_always=False, block_table=None, kv_layout="pthd",
-            mean_correction=False):
+            mean_correction=False, schedule="paired"):
     """Gated causal prefill.  Batched: q [B, Hq, L, d] (layout "bhld") or
     [B, L, Hq, d] ("blhd"); varlen (cu_seqlens int32 on the device): q [Hq, T, d]
     ("htd") or [T, Hq, d] ("thd").  Returns a dict with "out" and, on request,
@@ -221,7 +224,11 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
 
     ``mean_correction``: every skipped candidate block enters the softmax
     through a stand-in built from its mean key and mean value, weighted by its
-    key count (threshold and lambda modes, 128 x 128 blocks, contiguous K/V)."""
+    key count (threshold and lambda modes, 128 x 128 blocks, contiguous K/V).
+
+    ``schedule``: "paired" (two query heads of a GQA group per CTA, sharing
+    each K/V tile) or "pipelined" (one query head per CTA, Q.K^T of the next
+    tiles issued ahead of the current P.V; 128 x 128 blocks)."""
     if out is None:
         out = torch.empty_like(q)
     dev = q.device
@@ -230,7 +237,8 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
     p = _params(q, k, v, out, layout=layout, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
                 block_q=block_q, block_k=block_k, softmax_scale=softmax_scale, mode=mode,
                 thresholds=thresholds, log_lambda=log_lambda, v_always=v_always,
-                block_table=block_table, kv_layout=kv_layout, mean_correction=mean_correction)
+                block_table=block_table, kv_layout=kv_layout, mean_correction=mean_correction,
+                schedule=schedule)
     L = _native.lib()
     res = {"out": out}
     if return_bitmap:
@@ -271,7 +279,8 @@ def prefill_workspace_bytes(q, k, v, **kw) -> int:
                 thresholds=kw.get("thresholds"), log_lambda=kw.get("log_lambda"),
                 v_always=kw.get("v_always", False), block_table=kw.get("block_table"),
                 kv_layout=kw.get("kv_layout", "pthd"),
-                mean_correction=kw.get("mean_correction", False))
+                mean_correction=kw.get("mean_correction", False),
+                schedule=kw.get("schedule", "paired"))
     return int(_native.lib().bsfa_prefill_workspace_size(ctypes.byref(p)))
 
 

@@ -275,6 +275,25 @@ static cudaError_t dispatch_t(int d, int nq, Variant v, const Maps& m, const Dev
   }
 }
 
+// The pipelined schedule (bsfa_xs_kernel, BSFA_FLAG_PIPELINED): 128 x 128
+// semantic blocks, no mean correction.
+template <bool F16>
+static cudaError_t dispatch_xs_t(int d, Variant v, const Maps& m, const DevParams& p, int grid,
+                                 cudaStream_t st) {
+  if (d == 128) {
+    if (v.paged) return v.gating ? launch_xs<128, true, F16, false, true>(m, p, grid, st)
+                                 : launch_xs<128, false, F16, false, true>(m, p, grid, st);
+    if (v.gating && v.vall) return launch_xs<128, true, F16, true, false>(m, p, grid, st);
+    return v.gating ? launch_xs<128, true, F16, false, false>(m, p, grid, st)
+                    : launch_xs<128, false, F16, false, false>(m, p, grid, st);
+  }
+  if (v.paged) return v.gating ? launch_xs<64, true, F16, false, true>(m, p, grid, st)
+                               : launch_xs<64, false, F16, false, true>(m, p, grid, st);
+  if (v.gating && v.vall) return launch_xs<64, true, F16, true, false>(m, p, grid, st);
+  return v.gating ? launch_xs<64, true, F16, false, false>(m, p, grid, st)
+                  : launch_xs<64, false, F16, false, false>(m, p, grid, st);
+}
+
 template <bool CALIB>
 static cudaError_t dispatch(bool f16, int d, int nq, Variant v, const Maps& m,
                             const DevParams& p, int grid, cudaStream_t st) {
@@ -344,7 +363,12 @@ static bsfa_status validate(const bsfa_fwd_params* p) {
     return BSFA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return BSFA_ERR_UNSUPPORTED;
   if (p->dtype != BSFA_DTYPE_BF16 && p->dtype != BSFA_DTYPE_F16) return BSFA_ERR_UNSUPPORTED;
-  if (p->flags & ~static_cast<unsigned>(BSFA_FLAG_V_ALWAYS | BSFA_FLAG_MEAN_CORRECTION))
+  if (p->flags & ~static_cast<unsigned>(BSFA_FLAG_V_ALWAYS | BSFA_FLAG_MEAN_CORRECTION |
+                                        BSFA_FLAG_PIPELINED))
+    return BSFA_ERR_UNSUPPORTED;
+  // The pipelined schedule: 128 x 128 semantic blocks, no mean correction.
+  if ((p->flags & BSFA_FLAG_PIPELINED) &&
+      (p->block_q != TILE || p->block_k != TILE || (p->flags & BSFA_FLAG_MEAN_CORRECTION)))
     return BSFA_ERR_UNSUPPORTED;
   if ((p->block_q != 64 && p->block_q != 128) || (p->block_k != 64 && p->block_k != 128))
     return BSFA_ERR_UNSUPPORTED;
@@ -536,12 +560,20 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
           cv.seqinfo, cv.tiles, cv.ntot, cv.kbar, cv.vbar, (int)tb);
     if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;
   }
-  const long long units = tb * p->num_heads_kv * (g / nq);
   const int sms = num_sms();
   if (sms <= 0) return BSFA_ERR_CUDA;
-  const int grid = (int)(units < sms ? units : sms);
   const bool vall = (p->flags & BSFA_FLAG_V_ALWAYS) != 0;
   const Variant var{p->mode != BSFA_GATE_NONE, vall, paged, corr};
+  if (p->flags & BSFA_FLAG_PIPELINED) {
+    // One query head per CTA: units are (KV head, query tile, query head).
+    const long long units_xs = tb * p->num_heads_q;
+    const int grid_xs = (int)(units_xs < sms ? units_xs : sms);
+    const cudaError_t e = f16 ? dispatch_xs_t<true>(d, var, m, dp, grid_xs, stream)
+                              : dispatch_xs_t<false>(d, var, m, dp, grid_xs, stream);
+    return e == cudaSuccess ? BSFA_OK : BSFA_ERR_CUDA;
+  }
+  const long long units = tb * p->num_heads_kv * (g / nq);
+  const int grid = (int)(units < sms ? units : sms);
   if (dispatch<false>(f16, d, nq, var, m, dp, grid, stream) != cudaSuccess)
     return BSFA_ERR_CUDA;
   return BSFA_OK;

@@ -107,7 +107,19 @@ typedef enum {
    * head_dim * num_heads_kv <= 1024 (one thread per element in the block-mean
    * pass: Hkv <= 8 at d = 128, <= 16 at d = 64); else BSFA_ERR_UNSUPPORTED,
    * returned before anything is launched. */
-  BSFA_FLAG_MEAN_CORRECTION = 2
+  BSFA_FLAG_MEAN_CORRECTION = 2,
+  /* THRESHOLD, LAMBDA and NONE modes: the pipelined schedule instead of the
+   * paired one.  Same results up to rounding order (the gate's decisions and
+   * the bitmap are the same; outputs differ only in the fp32 summation order
+   * of the normaliser).  Paired (flags = 0): a CTA holds two query heads of
+   * one GQA group that share every K/V tile, with one score buffer each; a
+   * head's next Q.K^T waits for its current P.V.  Pipelined: a CTA holds one
+   * query head with two score buffers, so the Q.K^T of tile t + 2 is issued
+   * as soon as tile t's decision (a skip) or P (a keep) is in, ahead of its
+   * P.V ("Skipping attention blocks was the easy part", section "Cross-stage
+   * P").  Requires block_q == block_k == 128 and no mean correction, else
+   * BSFA_ERR_UNSUPPORTED.  Exists as a measured alternative schedule. */
+  BSFA_FLAG_PIPELINED = 4
 } bsfa_flag;
 
 /*

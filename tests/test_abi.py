@@ -68,8 +68,14 @@ def test_host_side_validation_without_gpu(libpath):
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unsupported block size
     p.block_k, p.dtype = 128, 7
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unknown element type
-    p.dtype, p.flags = _native.DTYPE_F16, 4
+    p.dtype, p.flags = _native.DTYPE_F16, 8
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # unknown flag bit
+    p.flags, p.block_k = _native.FLAG_PIPELINED, 64
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # pipelined: 128 x 128 blocks only
+    p.flags, p.block_k = _native.FLAG_PIPELINED | _native.FLAG_MEAN_CORRECTION, 128
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # pipelined: no mean correction
+    p.flags = _native.FLAG_PIPELINED
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # accepted up to the null tensors
     p.flags = _native.FLAG_V_ALWAYS
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # null tensors
     p.flags = 0

@@ -347,6 +347,7 @@ def run_ours(args, rank, world, local_rank):
         result["lambda_sweep"] = lambda_sweep(dev, args)
         result["llama8b_L32768"] = llama_32k_leg(dev)
         result["varlen_8seq_32layer"] = varlen_32layer_leg(dev)
+        result["tile_128x224"] = tile224_leg(dev)
     if not args.no_e2e and not sharded:
         result["e2e"] = e2e(q, k, v, slices, flops, Bq, Bk, args, dev)
     if not args.no_cpu and rank == 0 and world == 1 and not sharded:
@@ -559,6 +560,43 @@ def lambda_sweep(dev, args):
             "pipelined_over_paired": [round(r_["ms_pipelined"] / r_["ms"], 4) for r_ in rows],
             "schedules": "ms*: paired schedule (two query heads of a GQA group per CTA); "
                          "*_pipelined: one query head per CTA, next Q.K^T issued ahead of P.V"}
+
+
+def tile224_leg(dev, reps=3):
+    """The H100 port's 128 x 224 tile on the 64K lambda-sweep layer shape (32
+    query heads, 8 KV heads, d = 128): the lambda gate at dialled 0% and 50%
+    skip (key scale tiers drawn per 224-key block), and the gate compiled out.
+    Effective FLOPs count 2 * 128 * 224 * d per visible tile and again per
+    kept tile."""
+    import torch
+
+    import block_sparse_gated_gb300 as bsfa
+    from block_sparse_gated_gb300 import workloads as wl
+    cfg = _cfg("lambda-sweep-L65536")
+    Hq, Hkv, d, L = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["L"]
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    rows = []
+    for n, r in enumerate((0.0, 0.5)):
+        x = wl.layer_inputs(Hq, Hkv, L, d, wl.eval_seed(cfg["index"], 20 + n), dev, skip_rate=r,
+                            block=224)
+        q, k, v = x.q[None], x.k[None], x.v[None]
+        out = torch.empty_like(q)
+        ll = cfg["log_lambda"] if r > 0 else -math.inf
+        kw = dict(block_q=128, block_k=224, out=out, workspace=ws)
+        res = bsfa.prefill(q, k, v, mode="lambda", log_lambda=ll, return_counts=True, **kw)
+        torch.cuda.synchronize()
+        kc, cand, diag = res["counts"].cpu().tolist()
+        ms = _timed(lambda: bsfa.prefill(q, k, v, mode="lambda", log_lambda=ll, **kw), reps)
+        row = {"target_skip": r, "measured_skip": round(1 - kc / cand, 4), "ms": round(ms, 3),
+               "effective_tflops": round(2.0 * 128 * 224 * d * (cand + diag + kc + diag) /
+                                         (ms * 1e-3) / 1e12, 1)}
+        if r == 0:
+            row["ms_gate_compiled_out"] = round(_timed(lambda: bsfa.prefill(
+                q, k, v, mode="none", **kw), reps), 3)
+        rows.append(row)
+        del x, q, k, v, out
+    return {"workload": "lambda-sweep-L65536 shape, Bq=128 Bk=224", "rows": rows,
+            "kernel": "single-head kernel, one 224-column score buffer"}
 
 
 def _timed(fn, reps):

@@ -23,7 +23,7 @@ LIB = os.path.join(PKG, "libbsfa.so")
 
 SOURCES = ["bsfa_api.cu", "inst_fwd_d128.cu", "inst_fwd_d64.cu", "inst_fwd_vall.cu",
            "inst_calib.cu", "inst_fwd_paged_d128.cu", "inst_fwd_paged_d64.cu", "inst_fwd_corr.cu",
-           "bsfa_noalloc.cu", "inst_xs.cu"]
+           "bsfa_noalloc.cu", "inst_xs.cu", "inst_xs224.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -216,16 +216,17 @@ static EncodeTiled get_encoder() {
   return fn;
 }
 
-// 4-D map of 16-bit elements (bf16 or fp16) {d, tokens, heads, batch}, box {64, 128, 1, 1},
-// 128-byte swizzle.
+// 4-D map of 16-bit elements (bf16 or fp16) {d, tokens, heads, batch}, box {64, box_rows,
+// 1, 1} (128 rows, or 224 for the keys and values of the 128 x 224 tile), 128-byte swizzle.
 static bool make_map(CUtensorMap* m, const void* ptr, bool f16, int d, long long tokens, int heads,
-                     int batch, long long st_tok, long long st_head, long long st_batch) {
+                     int batch, long long st_tok, long long st_head, long long st_batch,
+                     int box_rows = TILE) {
   EncodeTiled enc = get_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)tokens, (cuuint64_t)heads, (cuuint64_t)batch};
   cuuint64_t strides[3] = {(cuuint64_t)st_tok * 2, (cuuint64_t)st_head * 2,
                            (cuuint64_t)st_batch * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)TILE, 1, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -277,21 +278,27 @@ static cudaError_t dispatch_t(int d, int nq, Variant v, const Maps& m, const Dev
 
 // The pipelined schedule (bsfa_xs_kernel, BSFA_FLAG_PIPELINED): 128 x 128
 // semantic blocks, no mean correction.
-template <bool F16>
-static cudaError_t dispatch_xs_t(int d, Variant v, const Maps& m, const DevParams& p, int grid,
+template <int D, int BK, bool F16>
+static cudaError_t dispatch_xs_d(Variant v, const Maps& m, const DevParams& p, int grid,
                                  cudaStream_t st) {
-  if (d == 128) {
-    if (v.paged) return v.gating ? launch_xs<128, true, F16, false, true>(m, p, grid, st)
-                                 : launch_xs<128, false, F16, false, true>(m, p, grid, st);
-    if (v.gating && v.vall) return launch_xs<128, true, F16, true, false>(m, p, grid, st);
-    return v.gating ? launch_xs<128, true, F16, false, false>(m, p, grid, st)
-                    : launch_xs<128, false, F16, false, false>(m, p, grid, st);
+  if constexpr (BK == 128) {
+    if (v.paged) return v.gating ? launch_xs<D, BK, true, false, F16, false, true>(m, p, grid, st)
+                                 : launch_xs<D, BK, false, false, F16, false, true>(m, p, grid, st);
   }
-  if (v.paged) return v.gating ? launch_xs<64, true, F16, false, true>(m, p, grid, st)
-                               : launch_xs<64, false, F16, false, true>(m, p, grid, st);
-  if (v.gating && v.vall) return launch_xs<64, true, F16, true, false>(m, p, grid, st);
-  return v.gating ? launch_xs<64, true, F16, false, false>(m, p, grid, st)
-                  : launch_xs<64, false, F16, false, false>(m, p, grid, st);
+  if (v.gating && v.vall) return launch_xs<D, BK, true, false, F16, true, false>(m, p, grid, st);
+  return v.gating ? launch_xs<D, BK, true, false, F16, false, false>(m, p, grid, st)
+                  : launch_xs<D, BK, false, false, F16, false, false>(m, p, grid, st);
+}
+
+// The single-head kernels: key tiles of 128 (BSFA_FLAG_PIPELINED) or 224.
+template <bool F16>
+static cudaError_t dispatch_xs_t(int d, int bk, Variant v, const Maps& m, const DevParams& p,
+                                 int grid, cudaStream_t st) {
+  if (bk == 224)
+    return d == 128 ? dispatch_xs_d<128, 224, F16>(v, m, p, grid, st)
+                    : dispatch_xs_d<64, 224, F16>(v, m, p, grid, st);
+  return d == 128 ? dispatch_xs_d<128, 128, F16>(v, m, p, grid, st)
+                  : dispatch_xs_d<64, 128, F16>(v, m, p, grid, st);
 }
 
 template <bool CALIB>
@@ -368,9 +375,17 @@ static bsfa_status validate(const bsfa_fwd_params* p) {
     return BSFA_ERR_UNSUPPORTED;
   // The pipelined schedule: 128 x 128 semantic blocks, no mean correction.
   if ((p->flags & BSFA_FLAG_PIPELINED) &&
-      (p->block_q != TILE || p->block_k != TILE || (p->flags & BSFA_FLAG_MEAN_CORRECTION)))
+      (p->block_q != TILE || (p->block_k != TILE && p->block_k != 224) ||
+       (p->flags & BSFA_FLAG_MEAN_CORRECTION)))
     return BSFA_ERR_UNSUPPORTED;
-  if ((p->block_q != 64 && p->block_q != 128) || (p->block_k != 64 && p->block_k != 128))
+  // Semantic blocks: Bq, Bk in {64, 128}, or the 128 x 224 tile.
+  const bool tile224 = p->block_q == TILE && p->block_k == 224;
+  if (!tile224 &&
+      ((p->block_q != 64 && p->block_q != 128) || (p->block_k != 64 && p->block_k != 128)))
+    return BSFA_ERR_UNSUPPORTED;
+  // The 128 x 224 tile: contiguous K/V (a 224-key tile would straddle pages)
+  // and no mean correction.
+  if (tile224 && (p->block_table != nullptr || (p->flags & BSFA_FLAG_MEAN_CORRECTION)))
     return BSFA_ERR_UNSUPPORTED;
   if (p->mode < BSFA_GATE_THRESHOLD || p->mode > BSFA_GATE_NONE) return BSFA_ERR_INVALID_ARG;
   if (p->batch > MAX_BATCH) return BSFA_ERR_UNSUPPORTED;
@@ -471,6 +486,7 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   };
   const bool f16 = p->dtype == BSFA_DTYPE_F16;
   const bool paged = p->block_table != nullptr;
+  const int kv_rows = p->block_k == 224 ? 224 : TILE;  // rows of one K or V tile
   if (!make_map(&m.q, p->q, f16, d, p->seqlen, p->num_heads_q, bdim, p->q_stride[2], p->q_stride[1],
                 bstride(p->q_stride, p->num_heads_q)))
     return BSFA_ERR_CUDA;
@@ -482,9 +498,9 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
                   p->v_stride[1], p->v_stride[0]))
       return BSFA_ERR_CUDA;
   } else if (!make_map(&m.k, p->k, f16, d, p->seqlen, p->num_heads_kv, bdim, p->k_stride[2],
-                       p->k_stride[1], bstride(p->k_stride, p->num_heads_kv)) ||
+                       p->k_stride[1], bstride(p->k_stride, p->num_heads_kv), kv_rows) ||
              !make_map(&m.v, p->v, f16, d, p->seqlen, p->num_heads_kv, bdim, p->v_stride[2],
-                       p->v_stride[1], bstride(p->v_stride, p->num_heads_kv))) {
+                       p->v_stride[1], bstride(p->v_stride, p->num_heads_kv), kv_rows)) {
     return BSFA_ERR_CUDA;
   }
   m.kb = m.k;
@@ -564,12 +580,12 @@ bsfa_status bsfa_prefill_fwd(const bsfa_fwd_params* p, bsfa_stream_t stream_) {
   if (sms <= 0) return BSFA_ERR_CUDA;
   const bool vall = (p->flags & BSFA_FLAG_V_ALWAYS) != 0;
   const Variant var{p->mode != BSFA_GATE_NONE, vall, paged, corr};
-  if (p->flags & BSFA_FLAG_PIPELINED) {
+  if ((p->flags & BSFA_FLAG_PIPELINED) || p->block_k == 224) {
     // One query head per CTA: units are (KV head, query tile, query head).
     const long long units_xs = tb * p->num_heads_q;
     const int grid_xs = (int)(units_xs < sms ? units_xs : sms);
-    const cudaError_t e = f16 ? dispatch_xs_t<true>(d, var, m, dp, grid_xs, stream)
-                              : dispatch_xs_t<false>(d, var, m, dp, grid_xs, stream);
+    const cudaError_t e = f16 ? dispatch_xs_t<true>(d, p->block_k, var, m, dp, grid_xs, stream)
+                              : dispatch_xs_t<false>(d, p->block_k, var, m, dp, grid_xs, stream);
     return e == cudaSuccess ? BSFA_OK : BSFA_ERR_CUDA;
   }
   const long long units = tb * p->num_heads_kv * (g / nq);
@@ -596,7 +612,9 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
   if (d != 64 && d != 128) return BSFA_ERR_UNSUPPORTED;
   if (dtype != BSFA_DTYPE_BF16 && dtype != BSFA_DTYPE_F16) return BSFA_ERR_UNSUPPORTED;
   const bool f16 = dtype == BSFA_DTYPE_F16;
-  if ((Bq != 64 && Bq != 128) || (Bk != 64 && Bk != 128)) return BSFA_ERR_UNSUPPORTED;
+  const bool tile224 = Bq == TILE && Bk == 224;  // the 128 x 224 tile
+  if (!tile224 && ((Bq != 64 && Bq != 128) || (Bk != 64 && Bk != 128)))
+    return BSFA_ERR_UNSUPPORTED;
   if (n_k > MAX_BUDGETS) return BSFA_ERR_UNSUPPORTED;
   for (int i = 0; i < n_k; ++i)
     if (ks[i] < 1) return BSFA_ERR_INVALID_ARG;
@@ -671,12 +689,24 @@ bsfa_status bsfa_calibrate(const void* const* q_samples, const void* const* k_sa
     if (!make_map(&m.q, q_samples[n], f16, d, L, Hq, 1, q_stride[1], q_stride[0],
                   (long long)q_stride[0] * Hq) ||
         !make_map(&m.k, k_samples[n], f16, d, L, Hkv, 1, k_stride[1], k_stride[0],
-                  (long long)k_stride[0] * Hkv))
+                  (long long)k_stride[0] * Hkv, tile224 ? 224 : TILE))
       return BSFA_ERR_CUDA;
     m.v = m.kb = m.vb = m.k;
-    if (dispatch<true>(f16, d, nq, Variant{true, false, false, false}, m, dp, grid, stream) !=
-        cudaSuccess)
-      return BSFA_ERR_CUDA;
+    cudaError_t e;
+    if (tile224) {
+      // The single-head calibration kernel: one 224-key tile per semantic block.
+      const long long units_xs = (long long)max_tiles * Hq;
+      const int grid_xs = (int)(units_xs < sms ? units_xs : sms);
+      if (d == 128)
+        e = f16 ? launch_xs<128, 224, true, true, true, false, false>(m, dp, grid_xs, stream)
+                : launch_xs<128, 224, true, true, false, false, false>(m, dp, grid_xs, stream);
+      else
+        e = f16 ? launch_xs<64, 224, true, true, true, false, false>(m, dp, grid_xs, stream)
+                : launch_xs<64, 224, true, true, false, false, false>(m, dp, grid_xs, stream);
+    } else {
+      e = dispatch<true>(f16, d, nq, Variant{true, false, false, false}, m, dp, grid, stream);
+    }
+    if (e != cudaSuccess) return BSFA_ERR_CUDA;
     sa.sample = n;
     select_kernel<<<dim3(nqb, Hq), sel_threads, sel_smem, stream>>>(sa);
     if (cudaGetLastError() != cudaSuccess) return BSFA_ERR_CUDA;

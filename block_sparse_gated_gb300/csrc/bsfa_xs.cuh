@@ -1,64 +1,75 @@
-// bsfa_xs.cuh -- the pipelined gated prefill kernel for 128 x 128 semantic
-// blocks: one query head per CTA, the scores of key tiles t and t+1 in two
-// TMEM buffers, so that Q.K^T of tile t+2 is issued as soon as tile t's gate
-// decision (a skip) or its P (a keep) is in.  The gate then sits on the
-// softmax warps' path only, not on the tensor pipe's: a run of skipped
-// tiles streams Q.K^T back to back.
+// bsfa_xs.cuh -- the single-head gated prefill kernel: one query head per
+// CTA, one 128-row query tile per unit, key tiles of BK = 128 or 224 keys,
+// each key tile one semantic block (Bq = 128, Bk = BK).
+//
+// BK = 128, the pipelined schedule: the scores of key tiles t and t+1 live in
+// two TMEM buffers, so Q.K^T of tile t+2 is issued as soon as tile t's gate
+// decision (a skip) or its P (a keep) is in ("Skipping attention blocks was
+// the easy part", section "Cross-stage P": the next tile's Q.K^T does not
+// wait for the current tile's P.V).
+//
+// BK = 224, the H100 deployment tile of "Block Sparse Flash Attention"
+// ("Loss & Training": a 128-row query tile and a 224-key tile): one 224-column
+// score buffer (two would not fit next to O in the 512 TMEM columns), so the
+// next Q.K^T follows the current decision or P.V.  Key Designs 2 notes that
+// a single j = i index does not map the diagonal for unequal tiles: a key
+// tile is a candidate when all its keys precede the query tile's first row,
+// and every other visible key tile is in the diagonal region (kept, masked).
 //
 // What it computes is the same gated, renormalised attention as
-// bsfa_fwd_kernel ("Block Sparse Flash Attention", Key Designs 2 and 3;
-// the lambda gate of "Skipping attention blocks was the easy part", section
-// "Vote, then skip"): every visible 128 x 128 tile's scores are computed,
-// the tile maximum (or each row's maximum against its running max) decides
-// the tile, and a skipped tile gets no V load, no exp and no P.V.  The
-// schedule follows that page's "Cross-stage P" section in spirit: the next
-// tile's Q.K^T does not wait for the current tile's P.V.
+// bsfa_fwd_kernel (Key Designs 2 and 3; the lambda gate of "Vote, then
+// skip"): every visible tile's scores are computed, the tile maximum (or
+// each row's maximum against its running max) decides the tile, and a
+// skipped tile gets no V load, no exp and no P.V.  With CALIB the kernel
+// only computes Q.K^T and records sigma * (tile maximum) of every candidate
+// tile (the calibration pass of Key Designs 1).
 //
-// Roles (384 threads, one CTA per SM, persistent over a heaviest-first
-// list of (KV head, query tile, query head) units):
-//   warp 0      TMA producer: Q per unit, K for every visible tile (3-stage
-//               ring), V for every tile when the gate is compiled out.
+// Roles (384 threads, one CTA per SM, persistent over a heaviest-first list
+// of (KV head, query tile, query head) units):
+//   warp 0      TMA producer: Q per unit, K for every visible tile, V for
+//               every tile when the gate is compiled out.
 //   warp 1      MMA issuer, TMEM owner.
 //   warp 3      (gate on) V loader: V of the tiles the gate keeps.
 //   warps 4-11  softmax: warp 4 + 4 ch + wq holds, for rows 32 wq .. 32 wq
-//               + 31, the tile's keys [64 ch, 64 ch + 64).
+//               + 31, the tile's keys [BK/2 ch, BK/2 ch + BK/2).
 //
-// TMEM: S buffers at columns [0, 128) and [128, 256) (tile t uses buffer
-// t % 2; P overwrites its first 64 columns as 16-bit pairs), O at [256,
-// 256 + D).
+// TMEM: score buffer b at columns [128 b, 128 b + BK) (P overwrites its first
+// BK/2 columns as 16-bit pairs), O at [256, 256 + D).
 #pragma once
 #include "bsfa_fwd.cuh"
 
 namespace bsfa {
 
-constexpr int XS_KST = 3;  // K ring stages (Q.K^T runs up to two tiles ahead)
-constexpr int XS_VST = 2;  // V ring stages
-
 struct XsCtrl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[XS_KST], k_empty[XS_KST];
-  uint64_t v_full[XS_VST], v_empty[XS_VST];
+  uint64_t k_full[3], k_empty[3];
+  uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2];    // per S buffer: scores of its current tile ready
-  uint64_t ph_full[2];   // per S buffer: P of keys 0-63 written (or tile skipped), 128 arrivals
-  uint64_t p_full[2];    // per S buffer: P of keys 64-127 written (or tile skipped), 128 arrivals
+  uint64_t ph_full[2];   // per S buffer: P of the first half of the keys written (or skipped)
+  uint64_t p_full[2];    // per S buffer: P of the second half written (or skipped)
   uint64_t dec_full[2];  // per S buffer: decision word published, 32 arrivals
-  uint64_t pv_done[2];   // per tile parity: that tile's P.V (if any) and all before it complete
+  uint64_t pv_done[2];   // per tile parity: that tile's P.V (if any) and all before it done
   uint64_t o_full, o_empty;
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t dec[2];       // per S buffer: tile stamp << DEC_BITS | keep bit
   float xmax[2][2][128]; // per (tile parity, column half, row): half-row maximum
   float xl[2][128];      // per (column half, row): share of the normaliser
+  float xw[2][8];        // calibration: per (tile parity, softmax warp) maximum
   int abort;
 };
 
-template <int D>
+template <int D, int BK, bool CALIB>
 struct XsLayout {
-  static constexpr int TB = TILE * D * 2;  // bytes of one 128-row 16-bit tile
+  static constexpr int NB = BK == 128 ? 2 : 1;                        // score buffers
+  static constexpr int KST = BK == 128 ? 3 : (D == 128 ? 1 : 2);      // K ring stages
+  static constexpr int VST = CALIB ? 0 : 2;                           // V ring stages
+  static constexpr int TQ = TILE * D * 2;  // bytes of the 128-row Q tile
+  static constexpr int TKV = BK * D * 2;   // bytes of one K or V tile
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + TB;
-  static constexpr int V_OFF = K_OFF + XS_KST * TB;
-  static constexpr int C_OFF = V_OFF + XS_VST * TB;
+  static constexpr int K_OFF = Q_OFF + TQ;
+  static constexpr int V_OFF = K_OFF + KST * TKV;
+  static constexpr int C_OFF = V_OFF + VST * TKV;
   static constexpr int RAW = C_OFF + (((int)sizeof(XsCtrl) + 15) & ~15) + 1024;
   // At least 120 KB, so that one CTA is resident per SM (the persistent grid
   // and the whole-TMEM allocation assume it).
@@ -66,6 +77,8 @@ struct XsLayout {
   static constexpr int NCOLS = 512;
   static constexpr int NTHREADS = 384;
   static constexpr uint32_t O_COL = 256;
+  static_assert(BYTES <= 227 * 1024, "shared memory");
+  static_assert(BK == 128 || BK == 224, "key tile");
 };
 
 // Signed distance, modulo the 28-bit decision stamp, of a decision word's
@@ -74,14 +87,47 @@ __device__ __forceinline__ int32_t xs_stamp_dist(uint32_t w, uint32_t tc) {
   return static_cast<int32_t>(((w >> DEC_BITS) - tc) << (32 - 28)) >> (32 - 28);
 }
 
-template <int D, bool GATING, bool F16, bool VALL, bool PAGED>
+// Key tiles visible to query tile I of a length-len sequence: those starting
+// at or before the tile's last row.
+template <int BK>
+__device__ __forceinline__ int xs_ntiles(int I, int len) {
+  return min(I * TILE + TILE - 1, len - 1) / BK + 1;
+}
+
+// S = Q K^T for one tile: D/16 K-steps of M = 128, N = BK, K = 16.  Q's and
+// K's 64-column swizzled halves sit TILE*128 and BK*128 bytes apart.
+template <int D, int BK>
+__device__ __forceinline__ void xs_issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk,
+                                            uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t oq = (((kk >> 2) * (TILE * 128)) + (kk & 3) * 32) >> 4;
+    const uint64_t ok = (((kk >> 2) * (BK * 128)) + (kk & 3) * 32) >> 4;
+    umma_ss(d_tmem, dq + oq, dk + ok, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V over K-steps [k0, k1) of 16 keys: P (16-bit pairs) in TMEM
+// columns [8 kk, 8 kk + 8) of the score buffer, V MN-major (16 keys = 2048 B
+// per 64-column half).
+__device__ __forceinline__ void xs_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv,
+                                            uint32_t idesc, uint32_t acc, int k0, int k1) {
+#pragma unroll
+  for (int kk = k0; kk < k1; ++kk)
+    umma_ts(d_tmem, p_tmem + kk * 8, dv + ((kk * 2048) >> 4), idesc, (kk > 0 || acc) ? 1u : 0u);
+}
+
+template <int D, int BK, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
 __global__ void __launch_bounds__(384, 1)
     bsfa_xs_kernel(const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const DevParams p) {
-  using LY = XsLayout<D>;
-  constexpr int TB = LY::TB;
-  constexpr int HALF = TILE * 128;  // bytes of one 64-column swizzled half
+  using LY = XsLayout<D, BK, CALIB>;
+  constexpr int NB = LY::NB, KST = LY::KST, VST = LY::VST;
+  constexpr int VSTN = VST > 0 ? VST : 1;  // divisor for V ring indices (no V ring: unused)
+  constexpr int TQ = LY::TQ, TKV = LY::TKV;
+  constexpr int QHALF = TILE * 128;  // bytes of one 64-column swizzled half of Q
+  constexpr int KHALF = BK * 128;    // the same for a K or V tile
   constexpr int NHALF = D / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -97,11 +143,11 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&c->q_full, 1);
     mbar_init(&c->q_empty, 1);
-    for (int i = 0; i < XS_KST; ++i) {
+    for (int i = 0; i < KST; ++i) {
       mbar_init(&c->k_full[i], 1);
       mbar_init(&c->k_empty[i], 1);
     }
-    for (int i = 0; i < XS_VST; ++i) {
+    for (int i = 0; i < VST; ++i) {
       mbar_init(&c->v_full[i], 1);
       mbar_init(&c->v_empty[i], 1);
     }
@@ -122,7 +168,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
+    if (!CALIB) prefetch_tensormap(&tmV);
   }
   if (warp == 1) {
     tmem_alloc(&c->tmem_base, LY::NCOLS);
@@ -150,40 +196,44 @@ __global__ void __launch_bounds__(384, 1)
       const int2 t = p.tiles[rem / p.group];
       const int h = kvh * p.group + rem % p.group;
       const int4 si = p.seqinfo[t.x];
-      const int n = t.y + 1;
+      const int n = xs_ntiles<BK>(t.y, si.y);
       if (!(ok = wait_all(&c->q_empty, (uc & 1) ^ 1, abort, p.err, ERR_WAIT_Q_EMPTY))) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&c->q_full, TB);
+        mbar_arrive_expect_tx(&c->q_full, TQ);
         for (int hf = 0; hf < NHALF; ++hf)
-          tma_load_4d(sQ + hf * HALF, &tmQ, &c->q_full, hf * 64, si.x + t.y * TILE, h, si.w);
+          tma_load_4d(sQ + hf * QHALF, &tmQ, &c->q_full, hf * 64, si.x + t.y * TILE, h, si.w);
       }
       __syncwarp();
       last_q = static_cast<int>(uc);
       for (int J = 0; J < n; ++J) {
+        // A K tile's coordinates: the sequence's token base, or (paged, BK =
+        // 128 only) its page from the block table.
+        const int2 cc = PAGED ? kv_tile_coord<PAGED>(p, si, t.x, J)
+                              : make_int2(si.x + J * BK, si.w);
         {
-          const uint32_t st = kc % XS_KST;
-          const int2 cc = kv_tile_coord<PAGED>(p, si, t.x, J);  // before the wait
-          if (!(ok = wait_all(&c->k_empty[st], ((kc / XS_KST) & 1) ^ 1, abort, p.err,
+          const uint32_t st = kc % KST;
+          if (!(ok = wait_all(&c->k_empty[st], ((kc / KST) & 1) ^ 1, abort, p.err,
                               ERR_WAIT_K_EMPTY)))
             break;
           if (elect_one()) {
-            mbar_arrive_expect_tx(&c->k_full[st], TB);
+            mbar_arrive_expect_tx(&c->k_full[st], TKV);
             for (int hf = 0; hf < NHALF; ++hf)
-              tma_load_4d(sK + st * TB + hf * HALF, &tmK, &c->k_full[st], hf * 64, cc.x, kvh, cc.y);
+              tma_load_4d(sK + st * TKV + hf * KHALF, &tmK, &c->k_full[st], hf * 64, cc.x, kvh,
+                          cc.y);
           }
           __syncwarp();
           ++kc;
         }
-        if constexpr (!GATING) {
-          const uint32_t st = vc % XS_VST;
-          const int2 cc = kv_tile_coord<PAGED>(p, si, t.x, J);
-          if (!(ok = wait_all(&c->v_empty[st], ((vc / XS_VST) & 1) ^ 1, abort, p.err,
+        if constexpr (!GATING && !CALIB) {
+          const uint32_t st = vc % VSTN;
+          if (!(ok = wait_all(&c->v_empty[st], ((vc / VSTN) & 1) ^ 1, abort, p.err,
                               ERR_WAIT_V_EMPTY)))
             break;
           if (elect_one()) {
-            mbar_arrive_expect_tx(&c->v_full[st], TB);
+            mbar_arrive_expect_tx(&c->v_full[st], TKV);
             for (int hf = 0; hf < NHALF; ++hf)
-              tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64, cc.x, kvh, cc.y);
+              tma_load_4d(sV + st * TKV + hf * KHALF, &tmV, &c->v_full[st], hf * 64, cc.x, kvh,
+                          cc.y);
           }
           __syncwarp();
           ++vc;
@@ -193,16 +243,18 @@ __global__ void __launch_bounds__(384, 1)
     if (!ok) {
       // Let every copy already issued land before the CTA can exit.
       if (last_q >= 0) drain_wait(&c->q_full, last_q & 1);
-      for (uint32_t i = 0; i < XS_KST && i < kc; ++i) {
+      for (uint32_t i = 0; i < KST && i < kc; ++i) {
         const uint32_t f = kc - 1 - i;
-        drain_wait(&c->k_full[f % XS_KST], (f / XS_KST) & 1);
+        drain_wait(&c->k_full[f % KST], (f / KST) & 1);
       }
-      for (uint32_t i = 0; i < XS_VST && i < vc; ++i) {
-        const uint32_t f = vc - 1 - i;
-        drain_wait(&c->v_full[f % XS_VST], (f / XS_VST) & 1);
+      if constexpr (VST > 0) {
+        for (uint32_t i = 0; i < static_cast<uint32_t>(VST) && i < vc; ++i) {
+          const uint32_t f = vc - 1 - i;
+          drain_wait(&c->v_full[f % VSTN], (f / VSTN) & 1);
+        }
       }
     }
-  } else if (GATING && warp == 3) {
+  } else if (GATING && !CALIB && warp == 3) {
     // ----------------------------------------------------- V loader (gated)
     // V of a tile is requested as soon as the softmax publishes a keep (with
     // VALL: for every tile, as soon as a stage is free).
@@ -212,9 +264,10 @@ __global__ void __launch_bounds__(384, 1)
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int4 si = p.seqinfo[t.x];
-      const int n = t.y + 1;
+      const int n = xs_ntiles<BK>(t.y, si.y);
       for (int J = 0; J < n; ++J, ++tc) {
-        const int2 cc = kv_tile_coord<PAGED>(p, si, t.x, J);  // before the waits
+        const int2 cc = PAGED ? kv_tile_coord<PAGED>(p, si, t.x, J)
+                              : make_int2(si.x + J * BK, si.w);  // before the waits
         bool need = VALL;
         if constexpr (!VALL) {
           // The decision word of the tile's S buffer carries the tile stamp.  A
@@ -223,58 +276,63 @@ __global__ void __launch_bounds__(384, 1)
           // decision overwrites the word) is issued only after that P.V.  Only
           // a word from an earlier tile needs the wait; then the barrier's
           // phase for this tile has not completed, so its parity is safe.
-          const uint32_t b = tc & 1;
+          const uint32_t b = tc % NB;
           uint32_t w = __shfl_sync(0xffffffffu, ld_acquire_u32(&c->dec[b]), 0);
           if (xs_stamp_dist(w, tc) < 0) {
-            if (!(ok = wait_all(&c->dec_full[b], (tc >> 1) & 1, abort, p.err, ERR_WAIT_DEC)))
+            if (!(ok = wait_all(&c->dec_full[b], (tc / NB) & 1, abort, p.err, ERR_WAIT_DEC)))
               break;
             w = __shfl_sync(0xffffffffu, ld_acquire_u32(&c->dec[b]), 0);
           }
           need = xs_stamp_dist(w, tc) == 0 && (w & DEC_MASK) != 0u;
         }
         if (!need) continue;
-        const uint32_t st = vc % XS_VST;
-        if (!(ok = wait_all(&c->v_empty[st], ((vc / XS_VST) & 1) ^ 1, abort, p.err,
+        const uint32_t st = vc % VSTN;
+        if (!(ok = wait_all(&c->v_empty[st], ((vc / VSTN) & 1) ^ 1, abort, p.err,
                             ERR_WAIT_V_EMPTY)))
           break;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&c->v_full[st], TB);
+          mbar_arrive_expect_tx(&c->v_full[st], TKV);
           for (int hf = 0; hf < NHALF; ++hf)
-            tma_load_4d(sV + st * TB + hf * HALF, &tmV, &c->v_full[st], hf * 64, cc.x, kvh, cc.y);
+            tma_load_4d(sV + st * TKV + hf * KHALF, &tmV, &c->v_full[st], hf * 64, cc.x, kvh,
+                        cc.y);
         }
         __syncwarp();
         ++vc;
       }
     }
     if (!ok) {
-      for (uint32_t i = 0; i < XS_VST && i < vc; ++i) {
-        const uint32_t f = vc - 1 - i;
-        drain_wait(&c->v_full[f % XS_VST], (f / XS_VST) & 1);
+      if constexpr (VST > 0) {
+        for (uint32_t i = 0; i < static_cast<uint32_t>(VST) && i < vc; ++i) {
+          const uint32_t f = vc - 1 - i;
+          drain_wait(&c->v_full[f % VSTN], (f / VSTN) & 1);
+        }
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
     // The whole warp runs the loop and the waits; one elected lane issues
-    // every MMA and commit.  Per unit: Q.K^T of tiles 0 and 1, then for each
-    // tile t: its decision; if kept, P.V (P in two halves); the commit of
-    // pv_done; then Q.K^T of tile t + 2 into t's S buffer (in issue order
-    // after t's P.V, which reads P from that buffer).
-    constexpr uint32_t IDESC_QK = idesc_f32acc<F16>(128, 128, false, false);
+    // every MMA and commit.  Per unit: Q.K^T of the first NB tiles, then for
+    // each tile t: its decision; if kept, P.V (P in two halves); the commit
+    // of pv_done; then Q.K^T of tile t + NB into t's score buffer (in issue
+    // order after t's P.V, which reads P from that buffer).  Calibration:
+    // the next Q.K^T follows the softmax's release of the buffer.
+    constexpr uint32_t IDESC_QK = idesc_f32acc<F16>(128, BK, false, false);
     constexpr uint32_t IDESC_PV = idesc_f32acc<F16>(128, D, false, true);
+    constexpr int KSTEPS = BK / 16, KHALFSTEPS = BK / 32;
     const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
-    const uint64_t dV = smem_desc_sw128(smem_u32(sV), HALF, 1024);
+    const uint64_t dV = smem_desc_sw128(smem_u32(sV), KHALF, 1024);
     const uint32_t d_o = tmem + LY::O_COL;
     uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
     bool ok = true;
-    // Q.K^T of the unit's tile j (j = tile index) into S buffer b.
+    // Q.K^T of the unit's tile j into score buffer b.
     auto issue_s = [&](int j, int n, uint32_t b) -> bool {
-      const uint32_t kst = kc % XS_KST;
-      if (!__all_sync(0xffffffffu, mbar_test_wait(&c->k_full[kst], (kc / XS_KST) & 1)) &&
-          !wait_all(&c->k_full[kst], (kc / XS_KST) & 1, abort, p.err, ERR_WAIT_K_FULL))
+      const uint32_t kst = kc % KST;
+      if (!__all_sync(0xffffffffu, mbar_test_wait(&c->k_full[kst], (kc / KST) & 1)) &&
+          !wait_all(&c->k_full[kst], (kc / KST) & 1, abort, p.err, ERR_WAIT_K_FULL))
         return false;
       if (elect_one()) {
-        issue_qk<D, 1>(tmem + b * 128, dQ, dK + ((kst * TB) >> 4), IDESC_QK);
+        xs_issue_qk<D, BK>(tmem + b * 128, dQ, dK + ((kst * TKV) >> 4), IDESC_QK);
         umma_commit(&c->s_full[b]);
         umma_commit(&c->k_empty[kst]);
         if (j == n - 1) umma_commit(&c->q_empty);
@@ -286,20 +344,28 @@ __global__ void __launch_bounds__(384, 1)
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
-      const int n = t.y + 1;
+      const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
       if (!(ok = wait_all(&c->q_full, uc & 1, abort, p.err, ERR_WAIT_Q_FULL))) break;
-      tc_fence_after();
-      for (int j = 0; j < 2 && j < n; ++j)
-        if (!(ok = issue_s(j, n, (tc + j) & 1))) break;
+      for (int j = 0; j < NB && j < n; ++j)
+        if (!(ok = issue_s(j, n, (tc + j) % NB))) break;
       if (!ok) break;
       bool first = true;  // no P.V of this unit issued yet
       for (int J = 0; J < n && ok; ++J, ++tc) {
-        const uint32_t b = tc & 1, ppar = (tc >> 1) & 1;
+        const uint32_t b = tc % NB, ppar = (tc / NB) & 1;
+        if constexpr (CALIB) {
+          // The softmax has read the scores (both halves arrive per tile).
+          if (!(ok = wait_all(&c->ph_full[b], ppar, abort, p.err, ERR_WAIT_P_FULL))) break;
+          if (!(ok = wait_all(&c->p_full[b], ppar, abort, p.err, ERR_WAIT_P_FULL))) break;
+          tc_fence_after();
+          if (J + NB < n && !(ok = issue_s(J + NB, n, b))) break;
+          continue;
+        }
         // Probe everything this step may need back to back (one shared-memory
-        // round trip), then block only on what is missing.
-        const uint32_t vst = vc % XS_VST;
-        // (warp-uniform: a phase counts as complete when every lane saw it so)
-        const bool v_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->v_full[vst], (vc / XS_VST) & 1));
+        // round trip), then block only on what is missing.  Warp-uniform: a
+        // phase counts as complete when every lane saw it so.
+        const uint32_t vst = vc % VSTN;
+        const bool v_ok =
+            __all_sync(0xffffffffu, mbar_test_wait(&c->v_full[vst], (vc / VSTN) & 1));
         const bool ph_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->ph_full[b], ppar));
         const bool p_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->p_full[b], ppar));
         bool keep = true;
@@ -314,7 +380,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         const bool vload = keep || (GATING && VALL);  // this tile's V stage was filled
         if (vload && !v_ok &&
-            !(ok = wait_all(&c->v_full[vst], (vc / XS_VST) & 1, abort, p.err, ERR_WAIT_V_FULL)))
+            !(ok = wait_all(&c->v_full[vst], (vc / VSTN) & 1, abort, p.err, ERR_WAIT_V_FULL)))
           break;
         if (keep) {
           if (PAGED && J == n - 1) {
@@ -322,7 +388,7 @@ __global__ void __launch_bounds__(384, 1)
             // hold anything there (NaN included), and P = 0 does not cancel
             // NaN in P.V.
             const int valid = p.seqinfo[t.x].y - J * TILE;
-            if (valid < TILE) zero_tile_rows<D>(sV + vst * TB, valid, lane);
+            if (valid < TILE) zero_tile_rows<D>(sV + vst * TKV, valid, lane);
           }
           uint32_t acc = 1u;
           if (first) {
@@ -332,21 +398,21 @@ __global__ void __launch_bounds__(384, 1)
             first = false;
           }
           const uint32_t d_p = tmem + b * 128;
-          const uint64_t dv_st = dV + ((vst * TB) >> 4);
+          const uint64_t dv_st = dV + ((vst * TKV) >> 4);
           if (ph_ok && p_ok) {
             tc_fence_after();
-            if (elect_one()) issue_pv<D, 1>(d_o, d_p, dv_st, IDESC_PV, acc);
+            if (elect_one()) xs_issue_pv(d_o, d_p, dv_st, IDESC_PV, acc, 0, KSTEPS);
             __syncwarp();
           } else {
             if (!ph_ok && !(ok = wait_all(&c->ph_full[b], ppar, abort, p.err, ERR_WAIT_P_FULL)))
               break;
             tc_fence_after();
-            if (elect_one()) issue_pv_half<D, 1>(d_o, d_p, dv_st, IDESC_PV, acc, 0);
+            if (elect_one()) xs_issue_pv(d_o, d_p, dv_st, IDESC_PV, acc, 0, KHALFSTEPS);
             __syncwarp();
             if (!p_ok && !(ok = wait_all(&c->p_full[b], ppar, abort, p.err, ERR_WAIT_P_FULL)))
               break;
             tc_fence_after();
-            if (elect_one()) issue_pv_half<D, 1>(d_o, d_p, dv_st, IDESC_PV, 1u, 1);
+            if (elect_one()) xs_issue_pv(d_o, d_p, dv_st, IDESC_PV, 1u, KHALFSTEPS, KSTEPS);
             __syncwarp();
           }
         } else {
@@ -360,11 +426,13 @@ __global__ void __launch_bounds__(384, 1)
         }
         __syncwarp();
         if (vload) ++vc;
-        if (J + 2 < n && !(ok = issue_s(J + 2, n, b))) break;
+        if (J + NB < n && !(ok = issue_s(J + NB, n, b))) break;
       }
       if (!ok) break;
-      if (elect_one()) umma_commit(&c->o_full);
-      __syncwarp();
+      if constexpr (!CALIB) {
+        if (elect_one()) umma_commit(&c->o_full);
+        __syncwarp();
+      }
     }
     // Drain: every issued MMA completes before TMEM can be released.
     if (elect_one()) umma_commit(&c->drain);
@@ -374,14 +442,16 @@ __global__ void __launch_bounds__(384, 1)
     // idle
   } else {
     // -------------------------------------------------------------- softmax
-    // Warp 4 + 4 ch + wq: rows 32 wq .. 32 wq + 31, keys [64 ch, 64 ch + 64)
-    // of each tile.  A thread loads its 64 scores once (the reducing TMEM
+    // Warp 4 + 4 ch + wq: rows 32 wq .. 32 wq + 31, keys [HK ch, HK ch + HK)
+    // of each tile.  A thread loads its HK scores once (the reducing TMEM
     // load also gives their maximum), votes, and takes its exp pass from
     // registers.  One barrier per tile joins the 256 softmax threads: its
     // count carries the gate's vote, the failure consensus and whether some
     // row needs the exact maximum of its two halves (a rise of the lazily
     // rescaled reference, or of the lambda running max); only then are the
     // half maxima exchanged through shared memory.
+    constexpr int HK = BK / 2, NCH = HK / 32, TAIL = HK % 32;  // TAIL is 0 or 16
+    static_assert(TAIL == 0 || TAIL == 16, "key split");
     const int ch = (warp - 4) >> 2;  // column half
     const int wq = warp & 3;         // TMEM lane quarter
     const int row = wq * 32 + lane;
@@ -391,12 +461,12 @@ __global__ void __launch_bounds__(384, 1)
     // Counts and bitmap words: every lane of warp 4 keeps them (lane 0 stores).
     const bool lead_warp = warp == 4;
     constexpr uint32_t bar_id = 1;
-    constexpr uint32_t NB = 256;
+    constexpr uint32_t NBAR = 256;
     const float sc = p.sigma_log2;
-    const bool lambda_mode = GATING && p.mode == 1;
+    const bool lambda_mode = GATING && !CALIB && p.mode == 1;
     uint32_t tc = 0, uc = 0;
     bool ok = true;
-    uint32_t cnt_kept = 0, cnt_cand = 0;
+    uint32_t cnt_kept = 0, cnt_cand = 0, cnt_diag = 0;
 
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
       int I, len, h;
@@ -407,9 +477,11 @@ __global__ void __launch_bounds__(384, 1)
         len = p.seqinfo[t.x].y;
         h = kvh * p.group + rem % p.group;
       }
-      const bool rvalid = I * TILE + row < len;
+      const int n = xs_ntiles<BK>(I, len);
+      const int rabs = I * TILE + row;  // my row's position in the sequence
+      const bool rvalid = rabs < len;
       float tq = 0.f;
-      if (GATING && p.mode == 0) tq = p.thr[(long long)h * p.nT + min(I, p.nT - 1)];
+      if (GATING && !CALIB && p.mode == 0) tq = p.thr[(long long)h * p.nT + min(I, p.nT - 1)];
       // m_used: reference of P (trails the running max by at most 2^8 in P
       // units); m_true: exact running max over kept blocks (lambda gate); l:
       // this half's share of the normaliser.
@@ -417,32 +489,59 @@ __global__ void __launch_bounds__(384, 1)
       bool o_init = false;
       uint32_t bm_word = 0;
 
-      for (int J = 0; J <= I; ++J, ++tc) {
-        const uint32_t b = tc & 1;
+      for (int J = 0; J < n; ++J, ++tc) {
+        const uint32_t b = tc % NB;
         // Every thread reaches the tile barrier below, also after its own
         // bounded wait gave up, so the 256 threads leave together.
-        const bool okl = wait_bar(&c->s_full[b], (tc >> 1) & 1, abort, p.err, ERR_WAIT_S_FULL);
+        const bool okl = wait_bar(&c->s_full[b], (tc / NB) & 1, abort, p.err, ERR_WAIT_S_FULL);
         __syncwarp();  // the TMEM loads below are warp-wide
         tc_fence_after();
-        const bool diag_tile = (J == I);
-        const uint32_t tS = tmem + tlane + b * 128 + ch * 64;  // my 64 score columns
+        // A candidate: every key precedes the query tile's first row; any
+        // other visible tile is in the diagonal region (kept, masked).
+        const bool cand = (J + 1) * BK <= I * TILE;
+        const int kbase = J * BK + ch * HK;  // position of my first key
+        const uint32_t tS = tmem + tlane + b * 128 + ch * HK;  // my score columns
 
-        // ---- my 64 scores and their maximum (masked on the diagonal tile)
-        uint32_t sr[2][32];
-        float lm;
+        // ---- my HK scores and their maximum (masked outside the candidates)
+        uint32_t sr[NCH][32];
+        uint32_t stl[16];
+        float lm = -CUDART_INF_F;
         {
-          float qm0, qm1;
-          tmem_ld32_max(tS, sr[0], qm0);
-          tmem_ld32_max(tS + 32, sr[1], qm1);
-          tmem_wait_ld();
-          if (!diag_tile) {
-            lm = fmaxf(qm0, qm1);
-          } else {
-            lm = -CUDART_INF_F;
+          float qm[NCH];
 #pragma unroll
-            for (int e = 0; e < 64; ++e)
-              if (ch * 64 + e <= row) lm = fmaxf(lm, __uint_as_float(sr[e >> 5][e & 31]));
+          for (int q = 0; q < NCH; ++q) tmem_ld32_max(tS + q * 32, sr[q], qm[q]);
+          if constexpr (TAIL > 0) tmem_ld16(tS + NCH * 32, stl);
+          tmem_wait_ld();
+          if (cand) {
+#pragma unroll
+            for (int q = 0; q < NCH; ++q) lm = fmaxf(lm, qm[q]);
+#pragma unroll
+            for (int e = 0; e < TAIL; ++e) lm = fmaxf(lm, __uint_as_float(stl[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < HK; ++e) {
+              const float x = __uint_as_float(e < NCH * 32 ? sr[e >> 5][e & 31] : stl[e & 15]);
+              if (kbase + e <= rabs) lm = fmaxf(lm, x);
+            }
           }
+        }
+
+        if constexpr (CALIB) {
+          // sigma * (tile maximum) of a candidate: the maximum over the valid
+          // rows of both halves, combined through shared memory.
+          const float wm = warp_max_f32(rvalid ? lm : -CUDART_INF_F);
+          if (lane == 0) c->xw[tc & 1][warp - 4] = wm;
+          tc_fence_before();
+          ok = bar_red_and(bar_id, NBAR, okl);
+          if (!ok) break;
+          if (cand && threadIdx.x == 128) {
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) mx = fmaxf(mx, c->xw[tc & 1][w]);
+            p.blockmax[((long long)h * p.cal_nq + I) * p.cal_nk + J] = mx * p.sigma;
+          }
+          mbar_arrive(ch == 0 ? &c->ph_full[b] : &c->p_full[b]);
+          continue;
         }
 
         // ---- votes.  Threshold: my half of the row wants the tile when
@@ -467,12 +566,12 @@ __global__ void __launch_bounds__(384, 1)
         // a row of the warp wants the tile (X, V <= 8).
         const bool wx = __any_sync(0xffffffffu, !okl || need_x);
         const bool wv = __any_sync(0xffffffffu, want);
-        const uint32_t n = bar_red_popc(bar_id, NB, lane == 0 ? wx : (lane <= 16 && wv));
-        const bool kept = !GATING || diag_tile || n >= 16u;
+        const uint32_t nv = bar_red_popc(bar_id, NBAR, lane == 0 ? wx : (lane <= 16 && wv));
+        const bool kept = !GATING || !cand || nv >= 16u;
         float rowmax = lm;  // the row's maximum over both halves (exact when exchanged)
-        if ((n & 15u) != 0u) {
+        if ((nv & 15u) != 0u) {
           c->xmax[tc & 1][ch][row] = lm;
-          ok = bar_red_and(bar_id, NB, okl);
+          ok = bar_red_and(bar_id, NBAR, okl);
           if (!ok) break;
           rowmax = fmaxf(lm, c->xmax[tc & 1][ch ^ 1][row]);
         }
@@ -484,7 +583,7 @@ __global__ void __launch_bounds__(384, 1)
 
         // ---- online softmax over my half of a kept tile
         if (kept) {
-          if ((n & 15u) != 0u) {  // rowmax is exact: rescale when the reference must rise
+          if ((nv & 15u) != 0u) {  // rowmax is exact: rescale when the reference must rise
             const float m_new = fmaxf(m_used, rowmax);
             const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
             float alpha = 1.f;
@@ -493,12 +592,12 @@ __global__ void __launch_bounds__(384, 1)
               m_used = m_new;
               l *= alpha;
             }
-            // O may still be accumulating the previous tile's P.V (Q.K^T of
-            // this tile was issued before it): wait until every P.V so far
-            // is done.  The TMEM loads and stores are warp-wide, so the warp
-            // rescales together, with alpha = 1 in rows that keep their
-            // reference.  A wait that gives up raises the abort flag, which
-            // the next tile barrier turns into a common exit.
+            // O may still be accumulating an earlier tile's P.V (with two
+            // score buffers this tile's Q.K^T was issued before it): wait
+            // until every P.V so far is done.  The TMEM loads and stores are
+            // warp-wide, so the warp rescales together, with alpha = 1 in rows
+            // that keep their reference.  A wait that gives up raises the
+            // abort flag, which the next tile barrier turns into a common exit.
             if (o_init && __any_sync(0xffffffffu, resc)) {
               wait_bar(&c->pv_done[(tc - 1) & 1], ((tc - 1) >> 1) & 1, abort, p.err,
                        ERR_WAIT_O_FULL);
@@ -517,19 +616,19 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
           // P = exp2(sigma*log2e*(S - m_used)) over my visible keys, packed as
-          // 16-bit pairs into my 32 P columns of the tile's S buffer.
-          const uint32_t tP = tmem + tlane + b * 128 + ch * 32;
+          // 16-bit pairs into my HK/2 P columns of the tile's score buffer.
+          const uint32_t tP = tmem + tlane + b * 128 + ch * (HK / 2);
           const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * sc;
           const uint64_t sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
           uint64_t lsum2 = f2_pack(0.f, 0.f);
 #pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {  // 32 of my keys per step, 16 P columns
+          for (int q = 0; q < NCH; ++q) {  // 32 of my keys per step, 16 P columns
             uint32_t pk[16];
-            if (!diag_tile) {
+            if (cand) {
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
-                const uint64_t x2 = f2_pack(__uint_as_float(sr[hq][2 * e]),
-                                            __uint_as_float(sr[hq][2 * e + 1]));
+                const uint64_t x2 = f2_pack(__uint_as_float(sr[q][2 * e]),
+                                            __uint_as_float(sr[q][2 * e + 1]));
                 float y0, y1;
                 f2_unpack(f2_fma(x2, sc2, nmb2), y0, y1);
                 const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
@@ -539,16 +638,30 @@ __global__ void __launch_bounds__(384, 1)
             } else {
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
-                const int key = ch * 64 + hq * 32 + 2 * e;
-                const float x0 = __uint_as_float(sr[hq][2 * e]);
-                const float x1 = __uint_as_float(sr[hq][2 * e + 1]);
-                const float p0 = key <= row ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
-                const float p1 = key + 1 <= row ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
+                const int key = kbase + q * 32 + 2 * e;
+                const float x0 = __uint_as_float(sr[q][2 * e]);
+                const float x1 = __uint_as_float(sr[q][2 * e + 1]);
+                const float p0 = key <= rabs ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
+                const float p1 = key + 1 <= rabs ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
                 lsum2 = f2_add(lsum2, f2_pack(p0, p1));
                 pk[e] = pack_x2<F16>(p0, p1);
               }
             }
-            tmem_st16(tP + hq * 16, pk);
+            tmem_st16(tP + q * 16, pk);
+          }
+          if constexpr (TAIL > 0) {  // the last 16 of my keys, 8 P columns
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int key = kbase + NCH * 32 + 2 * e;
+              const float x0 = __uint_as_float(stl[2 * e]);
+              const float x1 = __uint_as_float(stl[2 * e + 1]);
+              const float p0 = (cand || key <= rabs) ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
+              const float p1 = (cand || key + 1 <= rabs) ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
+              lsum2 = f2_add(lsum2, f2_pack(p0, p1));
+              pk[e] = pack_x2<F16>(p0, p1);
+            }
+            tmem_st8(tP + NCH * 16, pk);
           }
           float ls0, ls1;
           f2_unpack(lsum2, ls0, ls1);
@@ -557,18 +670,20 @@ __global__ void __launch_bounds__(384, 1)
           o_init = true;
         }
         // My half of P is written (or the tile skipped): one arrival per
-        // thread and tile on this half's barrier (keys 0-63: ph_full).
+        // thread and tile on this half's barrier (first half: ph_full).
         tc_fence_before();
         mbar_arrive(ch == 0 ? &c->ph_full[b] : &c->p_full[b]);
 
         // ---- bookkeeping: bitmap words and block counts (lead warp)
         if (lead_warp) {
-          if (!diag_tile) {
+          if (cand) {
             ++cnt_cand;
             cnt_kept += kept ? 1u : 0u;
+          } else {
+            ++cnt_diag;
           }
           if (kept) bm_word |= 1u << (J & 31);
-          if (p.bitmap != nullptr && ((J & 31) == 31 || diag_tile)) {
+          if (p.bitmap != nullptr && ((J & 31) == 31 || J == n - 1)) {
             const int4 si = p.seqinfo[p.tiles[(u % per_kv) / p.group].x];
             if (lane == 0)
               p.bitmap[((long long)(si.z + I) * p.Hq + h) * (long long)p.words + (J >> 5)] = bm_word;
@@ -577,24 +692,24 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (!ok) break;
+      if constexpr (CALIB) continue;
 
       // ---- epilogue: O / l -> 16-bit, log-sum-exp, bitmap tail
       const int4 si = p.seqinfo[p.tiles[(u % per_kv) / p.group].x];
       if (lead_warp && p.bitmap != nullptr) {
         const long long bm_row = ((long long)(si.z + I) * p.Hq + h) * (long long)p.words;
-        for (int w = (I >> 5) + 1 + lane; w < p.words; w += 32) p.bitmap[bm_row + w] = 0u;
+        for (int w = ((n - 1) >> 5) + 1 + lane; w < p.words; w += 32) p.bitmap[bm_row + w] = 0u;
       }
       c->xl[ch][row] = l;
       {
         const bool okl = wait_bar(&c->o_full, uc & 1, abort, p.err, ERR_WAIT_O_FULL);
-        if (!(ok = bar_red_and(bar_id, NB, okl))) break;
+        if (!(ok = bar_red_and(bar_id, NBAR, okl))) break;
       }
       tc_fence_after();
       const float lt = l + c->xl[ch ^ 1][row];
       const float inv_l = (lt > 0.f) ? 1.f / lt : 0.f;
-      const int qpos = I * TILE + row;
       uint16_t* orow = p.o + (long long)si.w * p.o_sb + (long long)h * p.o_sh +
-                       (long long)(si.x + qpos) * p.o_st + ch * DH;
+                       (long long)(si.x + rabs) * p.o_st + ch * DH;
 #pragma unroll
       for (int q = 0; q < DH / 16; ++q) {
         uint32_t orr[16];
@@ -614,16 +729,16 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (ch == 0 && p.lse != nullptr && rvalid)
         p.lse[(long long)h * p.lse_rows +
-              (p.varlen ? (long long)si.x : (long long)si.w * p.batch_len) + qpos] =
+              (p.varlen ? (long long)si.x : (long long)si.w * p.batch_len) + rabs] =
             m_used * p.sigma + logf(lt);
       // The next unit's first P.V overwrites O once all 256 threads are here.
       tc_fence_before();
       mbar_arrive(&c->o_empty);
     }
-    if (p.counts != nullptr && lead_warp && lane == 0 && uc != 0u) {
+    if (!CALIB && p.counts != nullptr && lead_warp && lane == 0 && (cnt_cand | cnt_diag) != 0u) {
       atomicAdd(&p.counts[0], (unsigned long long)cnt_kept);
       atomicAdd(&p.counts[1], (unsigned long long)cnt_cand);
-      atomicAdd(&p.counts[2], (unsigned long long)uc);  // one diagonal block per unit
+      atomicAdd(&p.counts[2], (unsigned long long)cnt_diag);
     }
   }
   tc_fence_before();

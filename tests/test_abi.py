@@ -76,6 +76,20 @@ def test_host_side_validation_without_gpu(libpath):
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # pipelined: no mean correction
     p.flags = _native.FLAG_PIPELINED
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # accepted up to the null tensors
+    # The 128 x 224 tile: accepted with 128-row query blocks only, contiguous
+    # K/V and no mean correction.
+    p.flags, p.block_q, p.block_k = 0, 128, 224
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # accepted up to the null tensors
+    p.block_q = 64
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2
+    p.block_q, p.flags = 128, _native.FLAG_MEAN_CORRECTION
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2
+    p.flags, p.block_table, p.block_table_stride, p.page_size, p.num_pages = 0, 1 << 12, 8, 256, 8
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2
+    p.block_table, p.block_table_stride, p.page_size, p.num_pages = None, 0, 0, 0
+    p.block_k = 160
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # no other key tile
+    p.block_k = 128
     p.flags = _native.FLAG_V_ALWAYS
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # null tensors
     p.flags = 0

@@ -152,7 +152,11 @@ typedef struct {
   int head_dim;               /* d: 64 or 128 */
   const int32_t* cu_seqlens;  /* device int32 [batch+1], nullable (batched layout) */
   int max_seqlen;             /* varlen: an upper bound on every sequence length */
-  int block_q, block_k;       /* semantic gate blocks Bq, Bk: each 64 or 128 */
+  int block_q, block_k;       /* semantic gate blocks Bq, Bk: each 64 or 128, or Bq = 128
+                                 with Bk = 224 (the H100 tile of the BSFA note, "Loss &
+                                 Training"; contiguous K/V and no mean correction, else
+                                 BSFA_ERR_UNSUPPORTED).  Any other pair:
+                                 BSFA_ERR_UNSUPPORTED */
   float softmax_scale;        /* sigma; <= 0 selects 1/sqrt(d) */
   int mode;                   /* bsfa_gate_mode */
   const float* thresholds;    /* device fp32 [Hq][thresholds_nq] (THRESHOLD mode): the
@@ -259,6 +263,7 @@ bsfa_status bsfa_prefill_fwd_noalloc(const bsfa_fwd_params* p, bsfa_stream_t str
  *     tensors (element type `dtype`, a bsfa_dtype) of one sample each, layout [H, L, d] addressed by the strides
  *     {head, token} in elements (d contiguous), equal L for every sample.
  *   ks: HOST array of n_k budgets (each >= 1).
+ *   block_q, block_k: 64 or 128 each, or 128 with 224.
  *   thresholds_out: device fp32 [n_k][Hq][ceil(L/Bq)], overwritten with the
  *     mean over samples of the k-th largest candidate block maximum (scaled
  *     by sigma), -inf where a sample has fewer than k candidates.

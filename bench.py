@@ -231,6 +231,16 @@ def aggregate_shards(ms_step, step_flops, world, device=None):
     return ms_step, step_flops / (ms_step * 1e-3) / 1e12, step_flops
 
 
+def _check_device(bsfa, what):
+    """Every kernel wait is bounded; one that ran out sets the device error
+    word and the kernel returns early, so its timing and outputs mean
+    nothing.  Refuse to report them."""
+    code = bsfa.api.device_error()
+    if code != 0:
+        raise RuntimeError(f"{what}: a device-side wait ran out (site {code:#x}); "
+                           "no number is reported")
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -291,6 +301,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clocks = clk.summary()
+    _check_device(bsfa, "timed step")
     total_ms = t_start.elapsed_time(t_end)
     step_flops = sum(flops)
     if sharded:
@@ -350,6 +361,7 @@ def run_ours(args, rank, world, local_rank):
         result["tile_128x224"] = tile224_leg(dev)
     if not args.no_e2e and not sharded:
         result["e2e"] = e2e(q, k, v, slices, flops, Bq, Bk, args, dev)
+    _check_device(bsfa, "bench legs")
     if not args.no_cpu and rank == 0 and world == 1 and not sharded:
         result["cpu_baseline"] = cpu_baseline(args.workload, W, cnts)
     if rank == 0:
@@ -520,14 +532,14 @@ def lambda_sweep(dev, args):
         x = wl.layer_inputs(Hq, Hkv, L, d, wl.eval_seed(cfg["index"], n), dev, skip_rate=r, block=B)
         q, k, v = x.q[None], x.k[None], x.v[None]
         out = torch.empty_like(q)
-        ll = cfg["log_lambda"] if r > 0 else -math.inf
+        ll = cfg["log_lambda"] if r > 0 else -1e30  # 0%: evaluated gate keeping every block
         res = bsfa.prefill(q, k, v, mode="lambda", log_lambda=ll, out=out, workspace=ws,
                            return_counts=True)
         torch.cuda.synchronize()
         kc, cand, diag = res["counts"].cpu().tolist()
         ms = timed(lambda: bsfa.prefill(q, k, v, mode="lambda", log_lambda=ll, out=out,
                                         workspace=ws))
-        row = {"target_skip": r, "log_lambda": ll if math.isfinite(ll) else "-inf",
+        row = {"target_skip": r, "log_lambda": ll,
                "measured_skip": round(1 - kc / cand, 4), "ms": round(ms, 3),
                "effective_tflops": round(effective_flops((kc, cand, diag), B, B, d) /
                                          (ms * 1e-3) / 1e12, 1),
@@ -538,12 +550,20 @@ def lambda_sweep(dev, args):
                    q, k, v, mode="lambda", log_lambda=ll, out=out, workspace=ws,
                    schedule="pipelined")), 3)}
         if r == 0:
-            thr = torch.full((Hq, 1), -math.inf, device=dev)
-            row["ms_threshold_minus_inf"] = round(timed(lambda: bsfa.prefill(
+            # The gate evaluated (threshold and ln(lambda) -1e30: every block
+            # kept after the vote), and -inf, which the kernel recognises as
+            # keep-everything without a vote.
+            thr = torch.full((Hq, 1), -1e30, device=dev)
+            thr_inf = torch.full((Hq, 1), -math.inf, device=dev)
+            row["ms_threshold_keep_all"] = round(timed(lambda: bsfa.prefill(
                 q, k, v, mode="threshold", thresholds=thr, out=out, workspace=ws)), 3)
+            row["ms_threshold_minus_inf"] = round(timed(lambda: bsfa.prefill(
+                q, k, v, mode="threshold", thresholds=thr_inf, out=out, workspace=ws)), 3)
+            row["ms_lambda_minus_inf"] = round(timed(lambda: bsfa.prefill(
+                q, k, v, mode="lambda", log_lambda=-math.inf, out=out, workspace=ws)), 3)
             row["ms_gate_compiled_out"] = round(timed(lambda: bsfa.prefill(
                 q, k, v, mode="none", out=out, workspace=ws)), 3)
-            row["ms_threshold_minus_inf_pipelined"] = round(timed(lambda: bsfa.prefill(
+            row["ms_threshold_keep_all_pipelined"] = round(timed(lambda: bsfa.prefill(
                 q, k, v, mode="threshold", thresholds=thr, out=out, workspace=ws,
                 schedule="pipelined")), 3)
             row["ms_gate_compiled_out_pipelined"] = round(timed(lambda: bsfa.prefill(
@@ -554,7 +574,14 @@ def lambda_sweep(dev, args):
     times = [r_["ms"] for r_ in rows]
     return {"workload": "lambda-sweep-L65536", "rows": rows,
             "zero_skip_overhead_lambda": round(rows[0]["ms"] / base - 1, 4),
-            "zero_skip_overhead_threshold": round(rows[0]["ms_threshold_minus_inf"] / base - 1, 4),
+            "zero_skip_overhead_threshold": round(rows[0]["ms_threshold_keep_all"] / base - 1, 4),
+            "zero_skip_overhead_minus_inf": {
+                "threshold": round(rows[0]["ms_threshold_minus_inf"] / base - 1, 4),
+                "lambda": round(rows[0]["ms_lambda_minus_inf"] / base - 1, 4),
+                "note": "a -inf threshold row (calibration gives one to query blocks with fewer "
+                        "than k candidates) or ln(lambda) = -inf keeps every block without a vote"},
+            "zero_skip_gate": "evaluated: threshold and ln(lambda) of -1e30 keep every block "
+                              "after the vote",
             "monotonic": all(a > b for a, b in zip(times, times[1:])),
             "v_always_over_gated_v": [round(r_["ms_v_always"] / r_["ms"], 4) for r_ in rows],
             "pipelined_over_paired": [round(r_["ms_pipelined"] / r_["ms"], 4) for r_ in rows],
@@ -581,7 +608,7 @@ def tile224_leg(dev, reps=3):
                             block=224)
         q, k, v = x.q[None], x.k[None], x.v[None]
         out = torch.empty_like(q)
-        ll = cfg["log_lambda"] if r > 0 else -math.inf
+        ll = cfg["log_lambda"] if r > 0 else -1e30  # 0%: evaluated gate keeping every block
         kw = dict(block_q=128, block_k=224, out=out, workspace=ws)
         res = bsfa.prefill(q, k, v, mode="lambda", log_lambda=ll, return_counts=True, **kw)
         torch.cuda.synchronize()

@@ -235,6 +235,12 @@ __device__ __forceinline__ uint32_t bar_red_popc(uint32_t id, uint32_t n, bool p
   return r;
 }
 
+// A compile-time bool as a value (to instantiate a generic lambda twice).
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
+
 // Semantic block class of key block j for query block i (length-L sequence):
 // 1 = candidate (every key precedes every row), 2 = diagonal region, 0 = none.
 __device__ __forceinline__ int block_class(int i, int j, int Bq, int Bk, int L) {
@@ -245,6 +251,62 @@ __device__ __forceinline__ int block_class(int i, int j, int Bq, int Bk, int L) 
   if ((j + 1) * Bk <= first_row) return 1;
   if (first_key <= last_row) return 2;
   return 0;
+}
+
+// Signed distance, modulo the 28-bit decision stamp, of a decision word's
+// stamp from tile counter tc (the initial word 0xFFFFFFFF reads as -1 at 0).
+__device__ __forceinline__ int32_t stamp_dist(uint32_t w, uint32_t tc) {
+  return static_cast<int32_t>(((w >> DEC_BITS) - tc) << (32 - 28)) >> (32 - 28);
+}
+
+// The decision word of tile tc (or a later one) of one slot and tile parity,
+// read by a whole warp.  The barrier completes once per publication of that
+// word, in tile order, so each try targets the phase right after the stamp the
+// word carries, whose predecessor has completed; the word is re-read after
+// every try, so a parity try that aliases a later phase (the publisher having
+// moved on meanwhile) only costs a retry, and a reader that ran ahead (through
+// units without votes) finds an older stamp and waits for it.  Bounded like
+// every other wait: on timeout it sets the error word and the abort flag and
+// *ok = false.
+template <int NW = 2>  // words in the ring: tile tc publishes into word tc % NW
+__device__ __forceinline__ uint32_t wait_decision(const uint32_t* word, uint64_t* bar,
+                                                  uint32_t tc, volatile int* abort,
+                                                  unsigned* err, bool* ok) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 0;; ++n) {
+    const uint32_t w = __shfl_sync(0xffffffffu, ld_acquire_u32(word), 0);
+    if (stamp_dist(w, tc) >= 0) return w;
+    // The word's tiles are published in order tc % NW, tc % NW + NW, ...;
+    // the initial word has no stamp, and its first publication is phase 0.
+    const uint32_t next = (w == 0xFFFFFFFFu) ? (tc % NW) : ((w >> DEC_BITS) + NW);
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, (next / NW) & 1u))) continue;
+    if ((n & 15u) == 15u) {
+      const bool give_up = *abort || globaltimer_ns() - t0 > WAIT_TIMEOUT_NS;
+      if (__any_sync(0xffffffffu, give_up)) {
+        if (!*abort) {
+          *abort = 1;
+          atomicCAS(err, 0u, static_cast<unsigned>(ERR_WAIT_DEC));
+        }
+        *ok = false;
+        return w;
+      }
+    }
+  }
+}
+
+// True when the gate keeps every block of query tile I of head h: its
+// threshold entries are all -inf (calibration gives -inf to query blocks with
+// fewer than k candidates), or ln(lambda) = -inf.  Such a unit needs no vote:
+// the softmax, the MMA warp and the V loader all take every decision as a
+// keep without exchanging it.
+__device__ __forceinline__ bool unit_gate_trivial(const DevParams& p, int h, int I) {
+  if (p.mode == 1) return p.log_lambda == -CUDART_INF_F;
+  if (p.mode != 0) return false;
+  const int QS = TILE / p.Bq;
+  const int iq = (I * TILE) / p.Bq;
+  for (int q = 0; q < QS; ++q)
+    if (p.thr[(long long)h * p.nT + min(iq + q, p.nT - 1)] != -CUDART_INF_F) return false;
+  return true;
 }
 
 // Zero rows [first_row, 128) of a 128-row tile in shared memory as TMA wrote
@@ -493,6 +555,13 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
         const int2 vc2 = (!CORR || J < nkt) ? kv_tile_coord<PAGED>(p, si, t.x, J) : make_int2(0, 0);
         for (int s = 0; s < NQ && ok; ++s) {
           if constexpr (!VALL) {
+            // Every decision phase is consumed in order, also in units whose
+            // gate keeps everything (their decisions are published as
+            // keeps): so this warp never runs ahead of the decisions, and
+            // it trails them by at most one tile -- it only blocks, besides
+            // here, on the V stage of a kept tile, whose P.V (and so every
+            // later decision of that slot) waits for that V.  The parity wait
+            // therefore never falls two phases behind.
             if (!(ok = wait_all(&c->dec_full[s][tc & 1], (tc >> 1) & 1, abort, p.err,
                                 ERR_WAIT_DEC)))
               break;
@@ -548,6 +617,13 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
       const int2 t = p.tiles[(u % per_kv) / p.pairs];
       const int nkt = t.y + 1;
       const int ntt = nkt + (CORR ? (t.y + TILE - 1) / TILE : 0);
+      // Slots whose gate keeps every block of this unit: no decision to read.
+      uint32_t triv = 0;
+      if constexpr (GATING && !CALIB && !CORR) {
+        const int h0 = (u / per_kv) * p.group + ((u % per_kv) % p.pairs) * NQ;
+        for (int s = 0; s < NQ; ++s)
+          if (unit_gate_trivial(p, h0 + s, t.y)) triv |= 1u << s;
+      }
       for (int s = 0; s < NQ && ok; ++s)
         ok = wait_all(&c->q_full[s], uc & 1, abort, p.err, ERR_WAIT_Q_FULL);
       if (!ok) break;
@@ -589,7 +665,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
           const uint32_t dw = (GATING && !CALIB) ? ld_acquire_u32(&c->dec[s][tb]) : 0u;
           if constexpr (!CALIB) {
             uint32_t dec = 1u;
-            if constexpr (GATING) {
+            if (GATING && !((triv >> s) & 1u)) {
               uint32_t w = dw;
               if ((w >> DEC_BITS) != (tc & DEC_STAMP_MASK)) {  // not published yet
                 if (!(ok = wait_all(&c->dec_full[s][tb], ppar, abort, p.err, ERR_WAIT_DEC))) break;
@@ -751,6 +827,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
         thr[0] = p.thr[(long long)h * p.nT + min(iq_base, p.nT - 1)];
         if (QS == 2) thr[1] = p.thr[(long long)h * p.nT + min(iq_base + 1, p.nT - 1)];
       }
+      // A unit whose gate keeps everything takes no vote and no per-tile
+      // barrier; a bounded wait that gives up inside it is carried to the
+      // unit's epilogue barrier (`failed`), where the warpgroup leaves together.
+      const bool trivial = GATING && !CALIB && !CORR && unit_gate_trivial(p, h, I);
+      bool failed = false;
       float m_used = -CUDART_INF_F, m_true = -CUDART_INF_F, l = 0.f;
       bool o_init = false;
       uint32_t bm_word = 0;
@@ -764,311 +845,323 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
       uint32_t* my_kbits = kbits + (s * 4 + wq) * CORR_WORDS;
       uint32_t kbit_acc = 0;
 
-      for (int J = 0; J < nkt; ++J, ++tc) {
-        const int tb = tc & 1;
-        const uint32_t ph = (tc >> 1) & 1u;  // phase parity of the per-tile-parity barriers
-        // Waits here are bounded.  In the gated kernel every thread joins the
-        // per-tile vote barrier even after its own wait gave up, and the
-        // barrier's count tells all of them, so the warpgroup leaves together
-        // (its named barriers can never strand a warp).  The other kernels use
-        // no named barrier in this loop: a warp that gives up leaves alone and
-        // the others' bounded waits see the abort flag.
-        bool okl;
-        if constexpr (GATING && !CALIB) {
-          okl = wait_bar(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL);
-        } else {
-          if (!(ok = wait_all(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL))) break;
-          okl = true;
-        }
-        tc_fence_after();
-        const bool diag_tile = (J == I);  // keys beyond a row exist only in the last tile
-
-        // ---- pass 1: row maxima of the two 64-key halves of S
-        float rm0 = -CUDART_INF_F, rm1 = -CUDART_INF_F;
-        uint32_t sr[4][32];
-        // Unconditional, even for a thread whose wait gave up (it then reads
-        // stale S from its own TMEM columns and the vote barrier stops the
-        // warpgroup): a per-thread guard around the .sync.aligned loads cost
-        // the gated kernel about 2% of its tile period.
-        {
-          // The reducing TMEM load returns each 32-column quarter's maximum
-          // along with the values, so a tile below the diagonal needs no
-          // max instructions at all; the diagonal tile masks and reduces the
-          // values itself.
-          float qm[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tmem_ld32_max(tS + q * 32, sr[q], qm[q]);
-          tmem_wait_ld();
-          if (!diag_tile) {
-            rm0 = fmaxf(qm[0], qm[1]);
-            rm1 = fmaxf(qm[2], qm[3]);
+      // The tile loop, compiled twice: once for units whose gate keeps
+      // everything (no vote, no per-tile barrier) and once for the rest,
+      // so that neither pays for the other's branches.
+      auto tile_loop = [&](auto triv_c) {
+        constexpr bool TRIV = decltype(triv_c)::value;
+        for (int J = 0; J < nkt; ++J, ++tc) {
+          const int tb = tc & 1;
+          const uint32_t ph = (tc >> 1) & 1u;  // phase parity of the per-tile-parity barriers
+          // Waits here are bounded.  In the gated kernel every thread joins the
+          // per-tile vote barrier even after its own wait gave up, and the
+          // barrier's count tells all of them, so the warpgroup leaves together
+          // (its named barriers can never strand a warp).  The other kernels use
+          // no named barrier in this loop: a warp that gives up leaves alone and
+          // the others' bounded waits see the abort flag.
+          bool okl;
+          if constexpr (GATING && !CALIB) {
+            okl = wait_bar(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL);
           } else {
-#pragma unroll
-            for (int e = 0; e < 128; ++e) {
-              const float x = (e > row) ? -CUDART_INF_F : __uint_as_float(sr[e >> 5][e & 31]);
-              if (e < 64) rm0 = fmaxf(rm0, x); else rm1 = fmaxf(rm1, x);
-            }
+            if (!(ok = wait_all(&c->s_full[s], tc & 1, abort, p.err, ERR_WAIT_S_FULL))) break;
+            okl = true;
           }
-          if (KS == 1) {
-            rm0 = fmaxf(rm0, rm1);
-            rm1 = rm0;
-          }
-        }
+          tc_fence_after();
+          const bool diag_tile = (J == I);  // keys beyond a row exist only in the last tile
 
-        // Block classes of the (query, key) sub-blocks of this tile.
-        int cls[2][2] = {{0, 0}, {0, 0}};
-        if (simple) {
-          cls[0][0] = diag_tile ? 2 : 1;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              if (q < QS && k < KS)
-                cls[q][k] = block_class(iq_base + q, (J * TILE) / p.Bk + k, p.Bq, p.Bk, len);
-        }
-
-        // ---- gate votes.  Threshold: row r wants key half k when
-        // sigma * rowmax_r(k) >= T.  The tile maximum clears T exactly when
-        // some row's maximum does (scaling by sigma > 0 is monotone in fp32),
-        // so the OR of the row votes equals comparing s_max(i,j) with T.
-        // Lambda: row r wants the first sub-block when
-        // sigma * (rowmax_r - m_r) >= ln(lambda).
-        const bool lambda_mode = GATING && !CALIB && p.mode == 1;
-        if constexpr (CALIB) {
-          const float w0 = warp_max_f32(rvalid ? rm0 : -CUDART_INF_F);
-          const float w1 = (KS == 1) ? w0 : warp_max_f32(rvalid ? rm1 : -CUDART_INF_F);
-          c->red[s][tb][wq][0] = w0;  // every lane: same value
-          c->red[s][tb][wq][1] = w1;
-          tc_fence_before();
-          mbar_arrive(&c->red_full[s][tb]);
-          // Calibration: the slot's first warp records sigma * s_max of each
-          // candidate block once every warp's maxima are in.
-          if (wq == 0) {
-            if (!(ok = wait_all(&c->red_full[s][tb], ph, abort, p.err, ERR_WAIT_RED))) break;
-            if (lane == 0) {
-              for (int q = 0; q < QS; ++q)
-                for (int k = 0; k < KS; ++k) {
-                  if (cls[q][k] != 1) continue;
-                  float mx = -CUDART_INF_F;
-                  for (int w = 0; w < 4; ++w)
-                    if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][tb][w][k]);
-                  const long long idx =
-                      ((long long)h * p.cal_nq + iq_base + q) * p.cal_nk + (J * TILE) / p.Bk + k;
-                  p.blockmax[idx] = mx * p.sigma;
-                }
-            }
-            __syncwarp();
-          }
-          mbar_arrive(&c->p_full[s][tb]);
-          continue;
-        } else {
-          // ---- gate: decide every sub-block of this tile
-          bool keep[2][2];
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int k = 0; k < 2; ++k) keep[q][k] = cls[q][k] != 0;
-          if constexpr (GATING) {
-            bool w0, w1 = false;
-            if (!lambda_mode) {
-              const float tq = (myqs ? thr[1] : thr[0]);
-              w0 = rvalid && rm0 * p.sigma >= tq;
-              w1 = rvalid && rm1 * p.sigma >= tq;
+          // ---- pass 1: row maxima of the two 64-key halves of S
+          float rm0 = -CUDART_INF_F, rm1 = -CUDART_INF_F;
+          uint32_t sr[4][32];
+          // Unconditional, even for a thread whose wait gave up (it then reads
+          // stale S from its own TMEM columns and the vote barrier stops the
+          // warpgroup): a per-thread guard around the .sync.aligned loads cost
+          // the gated kernel about 2% of its tile period.
+          {
+            // The reducing TMEM load returns each 32-column quarter's maximum
+            // along with the values, so a tile below the diagonal needs no
+            // max instructions at all; the diagonal tile masks and reduces the
+            // values itself.
+            float qm[4];
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32_max(tS + q * 32, sr[q], qm[q]);
+            tmem_wait_ld();
+            if (!diag_tile) {
+              rm0 = fmaxf(qm[0], qm[1]);
+              rm1 = fmaxf(qm[2], qm[3]);
             } else {
-              w0 = rvalid && (myqs ? cls[1][0] : cls[0][0]) == 1 &&
-                   ((rm0 - m_true) * p.sigma >= p.log_lambda);
+  #pragma unroll
+              for (int e = 0; e < 128; ++e) {
+                const float x = (e > row) ? -CUDART_INF_F : __uint_as_float(sr[e >> 5][e & 31]);
+                if (e < 64) rm0 = fmaxf(rm0, x); else rm1 = fmaxf(rm1, x);
+              }
             }
-            // Every read of S is complete here (tcgen05.wait::ld above); the
-            // fence orders it before the barrier, so that the MMA warp may
-            // overwrite S as soon as it reads a skip decision.
+            if (KS == 1) {
+              rm0 = fmaxf(rm0, rm1);
+              rm1 = rm0;
+            }
+          }
+
+          // Block classes of the (query, key) sub-blocks of this tile.
+          int cls[2][2] = {{0, 0}, {0, 0}};
+          if (simple) {
+            cls[0][0] = diag_tile ? 2 : 1;
+          } else {
+  #pragma unroll
+            for (int q = 0; q < 2; ++q)
+  #pragma unroll
+              for (int k = 0; k < 2; ++k)
+                if (q < QS && k < KS)
+                  cls[q][k] = block_class(iq_base + q, (J * TILE) / p.Bk + k, p.Bq, p.Bk, len);
+          }
+
+          // ---- gate votes.  Threshold: row r wants key half k when
+          // sigma * rowmax_r(k) >= T.  The tile maximum clears T exactly when
+          // some row's maximum does (scaling by sigma > 0 is monotone in fp32),
+          // so the OR of the row votes equals comparing s_max(i,j) with T.
+          // Lambda: row r wants the first sub-block when
+          // sigma * (rowmax_r - m_r) >= ln(lambda).
+          const bool lambda_mode = GATING && !CALIB && p.mode == 1;
+          if constexpr (CALIB) {
+            const float w0 = warp_max_f32(rvalid ? rm0 : -CUDART_INF_F);
+            const float w1 = (KS == 1) ? w0 : warp_max_f32(rvalid ? rm1 : -CUDART_INF_F);
+            c->red[s][tb][wq][0] = w0;  // every lane: same value
+            c->red[s][tb][wq][1] = w1;
             tc_fence_before();
-            if (simple) {
-              // One 128x128 semantic block per tile: the hardware barrier
-              // itself carries the vote (no shared-memory traffic, which
-              // queues behind the MMAs' operand reads).  Lane 0 of each warp
-              // counts 1 when some lane of the warp has stopped, lanes 1..8
-              // count 1 each when some row of the warp wants the block, so the
-              // count is F + 8 V with F, V <= 4.
-              const bool wf = __any_sync(0xffffffffu, !okl);
-              const bool wv = __any_sync(0xffffffffu, w0);
-              const uint32_t n = bar_red_popc(bar_id, 128, lane == 0 ? wf : (lane <= 8 && wv));
-              ok = (n & 7u) == 0u;
-              if (!ok) break;
-              if (!diag_tile) keep[0][0] = n >= 8u;
-            } else {
-              c->vote[s][tb][wq] = (__any_sync(0xffffffffu, w0) ? 1u : 0u) |
-                                   ((KS == 2 && __any_sync(0xffffffffu, w1)) ? 2u : 0u);
-              ok = bar_red_and(bar_id, 128, okl);
-              if (!ok) break;
-              // OR the warp votes of each query half (warps 0-1 hold rows 0-63).
-              const uint4 vv = *reinterpret_cast<const uint4*>(&c->vote[s][tb][0]);
-              uint32_t vq0 = vv.x | vv.y, vq1 = vv.z | vv.w;
-              if (QS == 1) vq0 = vq1 = vq0 | vq1;
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                if (cls[0][k] == 1) keep[0][k] = (vq0 >> k) & 1u;
-                if (cls[1][k] == 1) keep[1][k] = (vq1 >> k) & 1u;
+            mbar_arrive(&c->red_full[s][tb]);
+            // Calibration: the slot's first warp records sigma * s_max of each
+            // candidate block once every warp's maxima are in.
+            if (wq == 0) {
+              if (!(ok = wait_all(&c->red_full[s][tb], ph, abort, p.err, ERR_WAIT_RED))) break;
+              if (lane == 0) {
+                for (int q = 0; q < QS; ++q)
+                  for (int k = 0; k < KS; ++k) {
+                    if (cls[q][k] != 1) continue;
+                    float mx = -CUDART_INF_F;
+                    for (int w = 0; w < 4; ++w)
+                      if (QS == 1 || (w >> 1) == q) mx = fmaxf(mx, c->red[s][tb][w][k]);
+                    const long long idx =
+                        ((long long)h * p.cal_nq + iq_base + q) * p.cal_nk + (J * TILE) / p.Bk + k;
+                    p.blockmax[idx] = mx * p.sigma;
+                  }
               }
+              __syncwarp();
             }
-            if (lambda_mode) {
-              // Sub-blocks in ascending key order; a row's running max moves
-              // only with the blocks it keeps, so the second key half is voted
-              // on after the first half's decision.
-              if ((myqs ? keep[1][0] : keep[0][0])) m_true = fmaxf(m_true, rm0);
-              if (KS == 2) {
-                if (cls[0][1] == 1 || cls[1][1] == 1) {
-                  const bool v1 = rvalid && (myqs ? cls[1][1] : cls[0][1]) == 1 &&
-                                  ((rm1 - m_true) * p.sigma >= p.log_lambda);
-                  c->vote2[s][tb][wq] = __any_sync(0xffffffffu, v1) ? 1u : 0u;
-                  // Every thread passed the vote barrier above, so all of them
-                  // reach this one.
-                  named_bar_sync(bar_id, 128);
-                  const uint4 v2 = *reinterpret_cast<const uint4*>(&c->vote2[s][tb][0]);
-                  uint32_t u0 = v2.x | v2.y, u1 = v2.z | v2.w;
-                  if (QS == 1) u0 = u1 = u0 | u1;
-                  if (cls[0][1] == 1) keep[0][1] = u0 & 1u;
-                  if (cls[1][1] == 1) keep[1][1] = u1 & 1u;
+            mbar_arrive(&c->p_full[s][tb]);
+            continue;
+          } else {
+            // ---- gate: decide every sub-block of this tile
+            bool keep[2][2];
+  #pragma unroll
+            for (int q = 0; q < 2; ++q)
+  #pragma unroll
+              for (int k = 0; k < 2; ++k) keep[q][k] = cls[q][k] != 0;
+            if constexpr (GATING && TRIV) {
+              failed = failed || !okl;
+            } else if constexpr (GATING) {
+              bool w0, w1 = false;
+              if (!lambda_mode) {
+                const float tq = (myqs ? thr[1] : thr[0]);
+                w0 = rvalid && rm0 * p.sigma >= tq;
+                w1 = rvalid && rm1 * p.sigma >= tq;
+              } else {
+                w0 = rvalid && (myqs ? cls[1][0] : cls[0][0]) == 1 &&
+                     ((rm0 - m_true) * p.sigma >= p.log_lambda);
+              }
+              // Every read of S is complete here (tcgen05.wait::ld above); the
+              // fence orders it before the barrier, so that the MMA warp may
+              // overwrite S as soon as it reads a skip decision.
+              tc_fence_before();
+              if (simple) {
+                // One 128x128 semantic block per tile: the hardware barrier
+                // itself carries the vote (no shared-memory traffic, which
+                // queues behind the MMAs' operand reads).  Lane 0 of each warp
+                // counts 1 when some lane of the warp has stopped, lanes 1..8
+                // count 1 each when some row of the warp wants the block, so the
+                // count is F + 8 V with F, V <= 4.
+                const bool wf = __any_sync(0xffffffffu, !okl);
+                const bool wv = __any_sync(0xffffffffu, w0);
+                const uint32_t n = bar_red_popc(bar_id, 128, lane == 0 ? wf : (lane <= 8 && wv));
+                ok = (n & 7u) == 0u;
+                if (!ok) break;
+                if (!diag_tile) keep[0][0] = n >= 8u;
+              } else {
+                c->vote[s][tb][wq] = (__any_sync(0xffffffffu, w0) ? 1u : 0u) |
+                                     ((KS == 2 && __any_sync(0xffffffffu, w1)) ? 2u : 0u);
+                ok = bar_red_and(bar_id, 128, okl);
+                if (!ok) break;
+                // OR the warp votes of each query half (warps 0-1 hold rows 0-63).
+                const uint4 vv = *reinterpret_cast<const uint4*>(&c->vote[s][tb][0]);
+                uint32_t vq0 = vv.x | vv.y, vq1 = vv.z | vv.w;
+                if (QS == 1) vq0 = vq1 = vq0 | vq1;
+  #pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  if (cls[0][k] == 1) keep[0][k] = (vq0 >> k) & 1u;
+                  if (cls[1][k] == 1) keep[1][k] = (vq1 >> k) & 1u;
                 }
-                if ((myqs ? keep[1][1] : keep[0][1])) m_true = fmaxf(m_true, rm1);
+              }
+              if (lambda_mode) {
+                // Sub-blocks in ascending key order; a row's running max moves
+                // only with the blocks it keeps, so the second key half is voted
+                // on after the first half's decision.
+                if ((myqs ? keep[1][0] : keep[0][0])) m_true = fmaxf(m_true, rm0);
+                if (KS == 2) {
+                  if (cls[0][1] == 1 || cls[1][1] == 1) {
+                    const bool v1 = rvalid && (myqs ? cls[1][1] : cls[0][1]) == 1 &&
+                                    ((rm1 - m_true) * p.sigma >= p.log_lambda);
+                    c->vote2[s][tb][wq] = __any_sync(0xffffffffu, v1) ? 1u : 0u;
+                    // Every thread passed the vote barrier above, so all of them
+                    // reach this one.
+                    named_bar_sync(bar_id, 128);
+                    const uint4 v2 = *reinterpret_cast<const uint4*>(&c->vote2[s][tb][0]);
+                    uint32_t u0 = v2.x | v2.y, u1 = v2.z | v2.w;
+                    if (QS == 1) u0 = u1 = u0 | u1;
+                    if (cls[0][1] == 1) keep[0][1] = u0 & 1u;
+                    if (cls[1][1] == 1) keep[1][1] = u1 & 1u;
+                  }
+                  if ((myqs ? keep[1][1] : keep[0][1])) m_true = fmaxf(m_true, rm1);
+                }
               }
             }
-          }
-          uint32_t decbits = 0;
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              if (keep[q][k]) decbits |= 1u << (q * 2 + k);
-          if (GATING && wq == 0) {  // all 32 lanes: same value, 32 arrivals
-            // Release: a reader that sees this tile's stamp also sees every
-            // S read the decision depended on (the votes it waited for).
-            st_release_u32(&c->dec[s][tb], ((tc & DEC_STAMP_MASK) << DEC_BITS) | decbits);
-            mbar_arrive(&c->dec_full[s][tb]);
-          }
-
-          // ---- online softmax over the kept sub-blocks of this slot
-          if (decbits != 0u) {
-            const bool k0 = (myqs ? keep[1][0] : keep[0][0]);
-            const bool k1 = (KS == 1) ? k0 : (myqs ? keep[1][1] : keep[0][1]);
-            float rmk = -CUDART_INF_F;
-            if (k0) rmk = fmaxf(rmk, rm0);
-            if (k1) rmk = fmaxf(rmk, rm1);
-            const float m_new = fmaxf(m_used, rmk);
-            const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
-            float alpha = 1.f;
-            if (resc) {
-              alpha = ex2_approx((m_used - m_new) * sc);
-              m_used = m_new;
-              l *= alpha;
+            uint32_t decbits = 0;
+  #pragma unroll
+            for (int q = 0; q < 2; ++q)
+  #pragma unroll
+              for (int k = 0; k < 2; ++k)
+                if (keep[q][k]) decbits |= 1u << (q * 2 + k);
+            if (GATING && wq == 0) {  // all 32 lanes: same value, 32 arrivals
+              // Release: a reader that sees this tile's stamp also sees every
+              // S read the decision depended on (the votes it waited for).
+              st_release_u32(&c->dec[s][tb], ((tc & DEC_STAMP_MASK) << DEC_BITS) | decbits);
+              mbar_arrive(&c->dec_full[s][tb]);
             }
-            if (o_init && __any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-              for (int q = 0; q < D / 32; ++q) {
-                uint32_t orr[32];
-                tmem_ld32(tO + q * 32, orr);
+
+            // ---- online softmax over the kept sub-blocks of this slot
+            if (decbits != 0u) {
+              const bool k0 = (myqs ? keep[1][0] : keep[0][0]);
+              const bool k1 = (KS == 1) ? k0 : (myqs ? keep[1][1] : keep[0][1]);
+              float rmk = -CUDART_INF_F;
+              if (k0) rmk = fmaxf(rmk, rm0);
+              if (k1) rmk = fmaxf(rmk, rm1);
+              const float m_new = fmaxf(m_used, rmk);
+              const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
+              float alpha = 1.f;
+              if (resc) {
+                alpha = ex2_approx((m_used - m_new) * sc);
+                m_used = m_new;
+                l *= alpha;
+              }
+              if (o_init && __any_sync(0xffffffffu, resc)) {
+  #pragma unroll 1
+                for (int q = 0; q < D / 32; ++q) {
+                  uint32_t orr[32];
+                  tmem_ld32(tO + q * 32, orr);
+                  tmem_wait_ld();
+  #pragma unroll
+                  for (int e = 0; e < 32; ++e)
+                    orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                  tmem_st32(tO + q * 32, orr);
+                }
+              }
+              // Pass 2: P = exp2(sigma*log2e*(S - m)) for the kept, visible
+              // entries, packed as bf16 pairs into the first 64 columns of the
+              // S region (half hf -> P columns [32 hf, 32 hf + 32); those S
+              // columns have been read by then).
+              const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * sc;
+              const uint64_t sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
+              uint64_t lsum2 = f2_pack(0.f, 0.f);
+              const bool fast = !diag_tile && k0 && k1;
+  #pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const bool kk = (hf == 0) ? k0 : k1;
+                // Re-read this half of S from TMEM (cheaper than holding the
+                // whole row in registers across the gate).
+                tmem_ld32(tS + hf * 64, sr[2 * hf]);
+                tmem_ld32(tS + hf * 64 + 32, sr[2 * hf + 1]);
                 tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                tmem_st32(tO + q * 32, orr);
-              }
-            }
-            // Pass 2: P = exp2(sigma*log2e*(S - m)) for the kept, visible
-            // entries, packed as bf16 pairs into the first 64 columns of the
-            // S region (half hf -> P columns [32 hf, 32 hf + 32); those S
-            // columns have been read by then).
-            const float mb = (m_used == -CUDART_INF_F) ? 0.f : m_used * sc;
-            const uint64_t sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
-            uint64_t lsum2 = f2_pack(0.f, 0.f);
-            const bool fast = !diag_tile && k0 && k1;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const bool kk = (hf == 0) ? k0 : k1;
-              // Re-read this half of S from TMEM (cheaper than holding the
-              // whole row in registers across the gate).
-              tmem_ld32(tS + hf * 64, sr[2 * hf]);
-              tmem_ld32(tS + hf * 64 + 32, sr[2 * hf + 1]);
-              tmem_wait_ld();
-              uint32_t pk[32];
-              if (fast) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  const uint64_t x2 = f2_pack(__uint_as_float(sr[2 * hf + (e >> 4)][(2 * e) & 31]),
-                                              __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e + 1) & 31]));
-                  float y0, y1;
-                  f2_unpack(f2_fma(x2, sc2, nmb2), y0, y1);
-                  const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-                  const uint64_t pp = f2_pack(p0, p1);
-                  lsum2 = f2_add(lsum2, pp);
-                  pk[e] = pack_x2<F16>(p0, p1);
+                uint32_t pk[32];
+                if (fast) {
+  #pragma unroll
+                  for (int e = 0; e < 32; ++e) {
+                    const uint64_t x2 = f2_pack(__uint_as_float(sr[2 * hf + (e >> 4)][(2 * e) & 31]),
+                                                __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e + 1) & 31]));
+                    float y0, y1;
+                    f2_unpack(f2_fma(x2, sc2, nmb2), y0, y1);
+                    const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+                    const uint64_t pp = f2_pack(p0, p1);
+                    lsum2 = f2_add(lsum2, pp);
+                    pk[e] = pack_x2<F16>(p0, p1);
+                  }
+                } else {
+  #pragma unroll
+                  for (int e = 0; e < 32; ++e) {
+                    const int cc = hf * 64 + 2 * e;
+                    const bool vis0 = kk && !(diag_tile && cc > row);
+                    const bool vis1 = kk && !(diag_tile && cc + 1 > row);
+                    const float x0 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e) & 31]);
+                    const float x1 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e + 1) & 31]);
+                    const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
+                    const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
+                    lsum2 = f2_add(lsum2, f2_pack(p0, p1));
+                    pk[e] = pack_x2<F16>(p0, p1);
+                  }
                 }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                  const int cc = hf * 64 + 2 * e;
-                  const bool vis0 = kk && !(diag_tile && cc > row);
-                  const bool vis1 = kk && !(diag_tile && cc + 1 > row);
-                  const float x0 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e) & 31]);
-                  const float x1 = __uint_as_float(sr[2 * hf + (e >> 4)][(2 * e + 1) & 31]);
-                  const float p0 = vis0 ? ex2_approx(fmaf(x0, sc, -mb)) : 0.f;
-                  const float p1 = vis1 ? ex2_approx(fmaf(x1, sc, -mb)) : 0.f;
-                  lsum2 = f2_add(lsum2, f2_pack(p0, p1));
-                  pk[e] = pack_x2<F16>(p0, p1);
+                tmem_st32(tS + hf * 32, pk);
+                if (GATING && hf == 0) {  // hand off the first half of P
+                  tmem_wait_st();
+                  tc_fence_before();
+                  mbar_arrive(&c->ph_full[s][tb]);
                 }
               }
-              tmem_st32(tS + hf * 32, pk);
-              if (GATING && hf == 0) {  // hand off the first half of P
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&c->ph_full[s][tb]);
-              }
+              float ls0, ls1;
+              f2_unpack(lsum2, ls0, ls1);
+              l += ls0 + ls1;
+              tmem_wait_st();
+              o_init = true;
             }
-            float ls0, ls1;
-            f2_unpack(lsum2, ls0, ls1);
-            l += ls0 + ls1;
-            tmem_wait_st();
-            o_init = true;
-          }
-          if (GATING && decbits == 0u) mbar_arrive(&c->ph_full[s][tb]);  // one phase per tile
-          tc_fence_before();
-          mbar_arrive(&c->p_full[s][tb]);
+            if (GATING && decbits == 0u) mbar_arrive(&c->ph_full[s][tb]);  // one phase per tile
+            tc_fence_before();
+            mbar_arrive(&c->p_full[s][tb]);
 
-          // ---- bookkeeping: bitmap words and block counts (after the
-          // hand-off of P, off the path to the next MMA)
-          if constexpr (CORR) {
-            if (J < I) {  // a candidate: record whether this slot kept it
-              kbit_acc |= (keep[0][0] ? 1u : 0u) << (J & 31);
-              if ((J & 31) == 31 || J == I - 1) {
-                my_kbits[J >> 5] = kbit_acc;  // every lane: same value
-                kbit_acc = 0u;
+            // ---- bookkeeping: bitmap words and block counts (after the
+            // hand-off of P, off the path to the next MMA)
+            if constexpr (CORR) {
+              if (J < I) {  // a candidate: record whether this slot kept it
+                kbit_acc |= (keep[0][0] ? 1u : 0u) << (J & 31);
+                if ((J & 31) == 31 || J == I - 1) {
+                  my_kbits[J >> 5] = kbit_acc;  // every lane: same value
+                  kbit_acc = 0u;
+                }
               }
             }
-          }
-          if (lead_warp && my_i * p.Bq < len) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int cl = (myqs ? cls[1][k] : cls[0][k]);
-              if (cl == 0) continue;
-              const int j = (J * TILE) / p.Bk + k;
-              if (cl == 1) {
-                ++cnt_cand;
-                cnt_kept += (myqs ? keep[1][k] : keep[0][k]) ? 1 : 0;
-              } else {
-                ++cnt_diag;
-              }
-              if (bm_on) {
-                if ((j >> 5) != bm_idx) {
-                  if (lane == 0) p.bitmap[bm_row + bm_idx] = bm_word;
-                  bm_idx = j >> 5;
-                  bm_word = 0;
+            if (lead_warp && my_i * p.Bq < len) {
+  #pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int cl = (myqs ? cls[1][k] : cls[0][k]);
+                if (cl == 0) continue;
+                const int j = (J * TILE) / p.Bk + k;
+                if (cl == 1) {
+                  ++cnt_cand;
+                  cnt_kept += (myqs ? keep[1][k] : keep[0][k]) ? 1 : 0;
+                } else {
+                  ++cnt_diag;
                 }
-                if ((myqs ? keep[1][k] : keep[0][k])) bm_word |= 1u << (j & 31);
+                if (bm_on) {
+                  if ((j >> 5) != bm_idx) {
+                    if (lane == 0) p.bitmap[bm_row + bm_idx] = bm_word;
+                    bm_idx = j >> 5;
+                    bm_word = 0;
+                  }
+                  if ((myqs ? keep[1][k] : keep[0][k])) bm_word |= 1u << (j & 31);
+                }
               }
             }
           }
         }
-      }
+      };
+      if (trivial)
+        tile_loop(BoolC<true>{});
+      else
+        tile_loop(BoolC<false>{});
       if (!ok) break;
 
       if constexpr (CORR && GATING && !CALIB) {
@@ -1180,7 +1273,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, CALIB, CORR>::NTHREADS, 1)
             p.bitmap[bm_row + w] = (w == bm_idx) ? bm_word : 0u;
         if constexpr (GATING) {
           const bool okl = wait_bar(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL);
-          if (!(ok = bar_red_and(bar_id, 128, okl))) break;
+          if (!(ok = bar_red_and(bar_id, 128, okl && !failed))) break;
         } else {
           if (!(ok = wait_all(&c->o_full[s], uc & 1, abort, p.err, ERR_WAIT_O_FULL))) break;
         }

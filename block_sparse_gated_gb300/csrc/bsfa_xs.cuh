@@ -81,12 +81,6 @@ struct XsLayout {
   static_assert(BK == 128 || BK == 224, "key tile");
 };
 
-// Signed distance, modulo the 28-bit decision stamp, of a decision word's
-// stamp from tile counter tc (the initial word 0xFFFFFFFF reads as -1 at 0).
-__device__ __forceinline__ int32_t xs_stamp_dist(uint32_t w, uint32_t tc) {
-  return static_cast<int32_t>(((w >> DEC_BITS) - tc) << (32 - 28)) >> (32 - 28);
-}
-
 // Key tiles visible to query tile I of a length-len sequence: those starting
 // at or before the tile's last row.
 template <int BK>
@@ -273,17 +267,11 @@ __global__ void __launch_bounds__(384, 1)
           // The decision word of the tile's S buffer carries the tile stamp.  A
           // word stamped with a later tile also means a skip: a kept tile's
           // P.V waits for its V, and the next Q.K^T into that buffer (whose
-          // decision overwrites the word) is issued only after that P.V.  Only
-          // a word from an earlier tile needs the wait; then the barrier's
-          // phase for this tile has not completed, so its parity is safe.
+          // decision overwrites the word) is issued only after that P.V.
           const uint32_t b = tc % NB;
-          uint32_t w = __shfl_sync(0xffffffffu, ld_acquire_u32(&c->dec[b]), 0);
-          if (xs_stamp_dist(w, tc) < 0) {
-            if (!(ok = wait_all(&c->dec_full[b], (tc / NB) & 1, abort, p.err, ERR_WAIT_DEC)))
-              break;
-            w = __shfl_sync(0xffffffffu, ld_acquire_u32(&c->dec[b]), 0);
-          }
-          need = xs_stamp_dist(w, tc) == 0 && (w & DEC_MASK) != 0u;
+          const uint32_t w = wait_decision<NB>(&c->dec[b], &c->dec_full[b], tc, abort, p.err, &ok);
+          if (!ok) break;
+          need = stamp_dist(w, tc) == 0 && (w & DEC_MASK) != 0u;
         }
         if (!need) continue;
         const uint32_t st = vc % VSTN;

@@ -282,3 +282,73 @@ def test_v_always_is_bit_identical(cuda_device, mode, Bq, Bk, d):
     assert torch.equal(a["lse"], b["lse"])
     kept, cand = a["counts"].cpu().tolist()[:2]
     assert 0 < kept < cand
+
+
+# ------------------------------------------------- gates that keep everything
+def test_keep_all_gate_with_and_without_vote(cuda_device):
+    """A -inf threshold row (or ln(lambda) = -inf) keeps every block without
+    a vote; -1e30 keeps every block after one.  Both give the same bytes."""
+    Hq, Hkv, L, d = 4, 2, 1000, 128
+    x, q, k, v = _inputs(Hq, Hkv, L, d, 95, cuda_device, skip_rate=0.5)
+    a = _run(q, k, v, mode="threshold", thresholds=torch.full((Hq, 1), -math.inf, device=cuda_device))
+    b = _run(q, k, v, mode="threshold", thresholds=torch.full((Hq, 1), -1e30, device=cuda_device))
+    c = _run(q, k, v, mode="lambda", log_lambda=-math.inf)
+    d_ = _run(q, k, v, mode="lambda", log_lambda=-1e30)
+    for r in (b, c, d_):
+        for key in ("out", "lse", "bitmap", "counts"):
+            assert torch.equal(a[key], r[key]), key
+    kept, cand = a["counts"].cpu().tolist()[:2]
+    assert kept == cand
+
+
+def test_mixed_trivial_and_voting_units(cuda_device):
+    """Within one call, units whose threshold entries are all -inf (no vote)
+    next to units that vote, including the two query heads of one CTA (a
+    GQA pair) taking different paths: against the oracle."""
+    Hq, Hkv, L, d = 4, 2, 1300, 128
+    x = wl.layer_inputs(Hq, Hkv, L, d, 96, needles=2)
+    table = gu.median_table(gu.to64(x.q), gu.to64(x.k), 128, 128, gu.default_sigma(d))
+    table[0, ::2] = -np.inf        # head 0: every other query block without a vote
+    table[2, :] = -np.inf          # head 2: all -inf, its pair partner (head 3) votes
+    table[1, 5:] = -np.inf         # head 1: -inf from query block 5 on
+    ref = _threshold_case(cuda_device, Hq, Hkv, L, d, 128, 128, 96, table, needles=2)
+    cand = ref["candidate"]
+    assert (ref["keep"][3] & cand[3]).sum() < cand[3].sum()  # head 3 really gates
+
+
+def test_high_skip_soak_many_units_per_cta(cuda_device):
+    """About 94% of the candidates skipped, query blocks below the budget at
+    -inf (kept without a vote), many units per CTA, 20 back-to-back calls:
+    no bounded wait may run out (a softmax running through skipped tiles
+    ahead of the V loader must not confuse its decision reads), and every
+    call gives the same bytes."""
+    Hq, Hkv, L, d, kb = 32, 8, 16384, 128, 8
+    x, q, k, v = _inputs(Hq, Hkv, L, d, 97, cuda_device, needles=4, block=128)
+    b = _bsfa()
+    nq = L // 128
+    # Per-row budget kb from the oracle's block maxima of two heads; the
+    # other heads take the median of those rows (the schedule does not care
+    # which heads the values come from).
+    q64, k64 = gu.to64(x.q), gu.to64(x.k)
+    sigma = gu.default_sigma(d)
+    T = np.full((Hq, nq), -np.inf, dtype=np.float32)
+    for h in (0, 17):
+        sm = orc.block_maxima(q64[h], k64[h // 4], 128, 128, sigma)
+        for i in range(kb, nq):
+            T[h, i] = orc.kth_largest(list(sm[i][np.isfinite(sm[i])]), kb)
+    fill = np.median(T[[0, 17]][:, kb:])
+    T[:, kb:] = np.where(np.isfinite(T[:, kb:]), T[:, kb:], fill)
+    Td = torch.from_numpy(T).to(cuda_device)
+    first = b.prefill(q[None], k[None], v[None], mode="threshold", thresholds=Td,
+                      return_bitmap=True, return_counts=True)
+    torch.cuda.synchronize()
+    assert b.api.device_error() == 0
+    kept, cand = first["counts"].cpu().tolist()[:2]
+    assert 1 - kept / cand > 0.85
+    for _ in range(20):
+        r = b.prefill(q[None], k[None], v[None], mode="threshold", thresholds=Td,
+                      return_bitmap=True)
+        torch.cuda.synchronize()
+        assert b.api.device_error() == 0
+        assert torch.equal(r["out"], first["out"])
+        assert torch.equal(r["bitmap"], first["bitmap"])

@@ -279,17 +279,19 @@ def run_ours(args, rank, world, local_rank):
     cnts = [c.cpu().tolist() for c in counts]
     flops = [effective_flops(c, Bq, Bk, d) for c in cnts]
 
-    for _ in range(args.warmup):
-        for i in range(len(ks)):
-            call(i)
-    torch.cuda.synchronize()
     starts = [[torch.cuda.Event(enable_timing=True) for _ in ks] for _ in range(args.steps)]
     ends = [[torch.cuda.Event(enable_timing=True) for _ in ks] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
+        # Warm up after the sampler has started, so the GPU does not sit idle
+        # (and drop its clocks) between the warm-up and the timed steps.
+        for _ in range(args.warmup):
+            for i in range(len(ks)):
+                call(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         t_start.record(stream)
         for s in range(args.steps):
             for i in range(len(ks)):

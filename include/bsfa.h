@@ -117,8 +117,11 @@ typedef enum {
    * query head with two score buffers, so the Q.K^T of tile t + 2 is issued
    * as soon as tile t's decision (a skip) or P (a keep) is in, ahead of its
    * P.V ("Skipping attention blocks was the easy part", section "Cross-stage
-   * P").  Requires block_q == block_k == 128 and no mean correction, else
-   * BSFA_ERR_UNSUPPORTED.  Exists as a measured alternative schedule. */
+   * P").  Requires block_q == 128, block_k == 128 or 224, and no mean
+   * correction, else BSFA_ERR_UNSUPPORTED.  Exists as a measured alternative
+   * schedule.  The 128 x 224 tile always runs one query head per CTA (its
+   * 224-column score buffer fits TMEM once, not twice), with or without this
+   * flag. */
   BSFA_FLAG_PIPELINED = 4
 } bsfa_flag;
 

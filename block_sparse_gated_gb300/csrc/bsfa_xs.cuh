@@ -2,11 +2,12 @@
 // CTA, one 128-row query tile per unit, key tiles of BK = 128 or 224 keys,
 // each key tile one semantic block (Bq = 128, Bk = BK).
 //
-// BK = 128, the pipelined schedule: the scores of key tiles t and t+1 live in
-// two TMEM buffers, so Q.K^T of tile t+2 is issued as soon as tile t's gate
-// decision (a skip) or its P (a keep) is in ("Skipping attention blocks was
-// the easy part", section "Cross-stage P": the next tile's Q.K^T does not
-// wait for the current tile's P.V).
+// BK = 128, the pipelined schedule: the scores of key tiles t, t+1 and t+2
+// live in three TMEM buffers, so Q.K^T of tile t+3 is issued as soon as tile
+// t's gate decision (a skip) or its P (a keep) is in ("Skipping attention
+// blocks was the easy part", section "Cross-stage P": the next tile's Q.K^T
+// does not wait for the current tile's P.V).  Two tiles' Q.K^T then run
+// while a third is being decided, which is what a run of skipped tiles needs.
 //
 // BK = 224, the H100 deployment tile of "Block Sparse Flash Attention"
 // ("Loss & Training": a 128-row query tile and a 224-key tile): one 224-column
@@ -26,15 +27,15 @@
 //
 // Roles (384 threads, one CTA per SM, persistent over a heaviest-first list
 // of (KV head, query tile, query head) units):
-//   warp 0      TMA producer: Q per unit, K for every visible tile, V for
-//               every tile when the gate is compiled out.
+//   warp 0      TMA producer: Q per unit, K for every visible tile.
 //   warp 1      MMA issuer, TMEM owner.
-//   warp 3      (gate on) V loader: V of the tiles the gate keeps.
+//   warp 3      V loader: V of the tiles the gate keeps (of every tile when
+//               the gate is compiled out or with VALL).
 //   warps 4-11  softmax: warp 4 + 4 ch + wq holds, for rows 32 wq .. 32 wq
 //               + 31, the tile's keys [BK/2 ch, BK/2 ch + BK/2).
 //
 // TMEM: score buffer b at columns [128 b, 128 b + BK) (P overwrites its first
-// BK/2 columns as 16-bit pairs), O at [256, 256 + D).
+// BK/2 columns as 16-bit pairs), O after them (XsLayout::O_COL).
 #pragma once
 #include "bsfa_fwd.cuh"
 
@@ -42,17 +43,17 @@ namespace bsfa {
 
 struct XsCtrl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[3], k_empty[3];
-  uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2];    // per S buffer: scores of its current tile ready
-  uint64_t ph_full[2];   // per S buffer: P of the first half of the keys written (or skipped)
-  uint64_t p_full[2];    // per S buffer: P of the second half written (or skipped)
-  uint64_t dec_full[2];  // per S buffer: decision word published, 32 arrivals
+  uint64_t k_full[4], k_empty[4];  // K ring (XsLayout::KST <= 4 stages)
+  uint64_t v_full[2], v_empty[2];  // V ring (XsLayout::VST <= 2 stages)
+  uint64_t s_full[3];    // per S buffer: scores of its current tile ready
+  uint64_t ph_full[3];   // per S buffer: P of the first half of the keys written (or skipped)
+  uint64_t p_full[3];    // per S buffer: P of the second half written (or skipped)
+  uint64_t dec_full[3];  // per S buffer: decision word published, 32 arrivals
   uint64_t pv_done[2];   // per tile parity: that tile's P.V (if any) and all before it done
   uint64_t o_full, o_empty;
   uint64_t drain;
   uint32_t tmem_base;
-  uint32_t dec[2];       // per S buffer: tile stamp << DEC_BITS | keep bit
+  uint32_t dec[3];       // per S buffer: tile stamp << DEC_BITS | keep bit
   float xmax[2][2][128]; // per (tile parity, column half, row): half-row maximum
   float xl[2][128];      // per (column half, row): share of the normaliser
   float xw[2][8];        // calibration: per (tile parity, softmax warp) maximum
@@ -61,7 +62,7 @@ struct XsCtrl {
 
 template <int D, int BK, bool CALIB>
 struct XsLayout {
-  static constexpr int NB = BK == 128 ? 2 : 1;                        // score buffers
+  static constexpr int NB = BK == 128 ? 3 : 1;                        // score buffers
   static constexpr int KST = BK == 128 ? 3 : (D == 128 ? 1 : 2);      // K ring stages
   static constexpr int VST = CALIB ? 0 : 2;                           // V ring stages
   static constexpr int TQ = TILE * D * 2;  // bytes of the 128-row Q tile
@@ -76,9 +77,13 @@ struct XsLayout {
   static constexpr int BYTES = RAW > 120 * 1024 ? RAW : 120 * 1024;
   static constexpr int NCOLS = 512;
   static constexpr int NTHREADS = 384;
-  static constexpr uint32_t O_COL = 256;
+  // O after the score buffers: [384, 384 + D) with three 128-column buffers,
+  // [256, 256 + D) after the single 224-column one.
+  static constexpr uint32_t O_COL = BK == 128 ? NB * 128 : 256;
+  static_assert(O_COL + D <= NCOLS, "TMEM columns");
   static_assert(BYTES <= 227 * 1024, "shared memory");
   static_assert(BK == 128 || BK == 224, "key tile");
+  static_assert(KST <= 4 && VST <= 2 && NB <= 3, "ring sizes of XsCtrl");
 };
 
 // Key tiles visible to query tile I of a length-len sequence: those starting
@@ -145,14 +150,14 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&c->v_full[i], 1);
       mbar_init(&c->v_empty[i], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       mbar_init(&c->s_full[b], 1);
       mbar_init(&c->ph_full[b], 128);
       mbar_init(&c->p_full[b], 128);
       mbar_init(&c->dec_full[b], 32);
-      mbar_init(&c->pv_done[b], 1);
       c->dec[b] = 0xFFFFFFFFu;  // no stamp matches
     }
+    for (int b = 0; b < 2; ++b) mbar_init(&c->pv_done[b], 1);
     mbar_init(&c->o_full, 1);
     mbar_init(&c->o_empty, 256);
     mbar_init(&c->drain, 1);
@@ -182,7 +187,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    uint32_t kc = 0, vc = 0, uc = 0;
+    uint32_t kc = 0, uc = 0;
     int last_q = -1;  // index of the last unit whose Q load was issued
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
@@ -218,20 +223,6 @@ __global__ void __launch_bounds__(384, 1)
           __syncwarp();
           ++kc;
         }
-        if constexpr (!GATING && !CALIB) {
-          const uint32_t st = vc % VSTN;
-          if (!(ok = wait_all(&c->v_empty[st], ((vc / VSTN) & 1) ^ 1, abort, p.err,
-                              ERR_WAIT_V_EMPTY)))
-            break;
-          if (elect_one()) {
-            mbar_arrive_expect_tx(&c->v_full[st], TKV);
-            for (int hf = 0; hf < NHALF; ++hf)
-              tma_load_4d(sV + st * TKV + hf * KHALF, &tmV, &c->v_full[st], hf * 64, cc.x, kvh,
-                          cc.y);
-          }
-          __syncwarp();
-          ++vc;
-        }
       }
     }
     if (!ok) {
@@ -241,17 +232,12 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t f = kc - 1 - i;
         drain_wait(&c->k_full[f % KST], (f / KST) & 1);
       }
-      if constexpr (VST > 0) {
-        for (uint32_t i = 0; i < static_cast<uint32_t>(VST) && i < vc; ++i) {
-          const uint32_t f = vc - 1 - i;
-          drain_wait(&c->v_full[f % VSTN], (f / VSTN) & 1);
-        }
-      }
     }
-  } else if (GATING && !CALIB && warp == 3) {
-    // ----------------------------------------------------- V loader (gated)
+  } else if (!CALIB && warp == 3) {
+    // ------------------------------------------------------------ V loader
     // V of a tile is requested as soon as the softmax publishes a keep (with
-    // VALL: for every tile, as soon as a stage is free).
+    // VALL, or with the gate compiled out: for every tile, as soon as a stage
+    // is free).  A warp of its own, so that K loads never queue behind V.
     uint32_t vc = 0, tc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
@@ -262,8 +248,8 @@ __global__ void __launch_bounds__(384, 1)
       for (int J = 0; J < n; ++J, ++tc) {
         const int2 cc = PAGED ? kv_tile_coord<PAGED>(p, si, t.x, J)
                               : make_int2(si.x + J * BK, si.w);  // before the waits
-        bool need = VALL;
-        if constexpr (!VALL) {
+        bool need = VALL || !GATING;
+        if constexpr (GATING && !VALL) {
           // The decision word of the tile's S buffer carries the tile stamp.  A
           // word stamped with a later tile also means a skip: a kept tile's
           // P.V waits for its V, and the next Q.K^T into that buffer (whose
@@ -580,7 +566,7 @@ __global__ void __launch_bounds__(384, 1)
               m_used = m_new;
               l *= alpha;
             }
-            // O may still be accumulating an earlier tile's P.V (with two
+            // O may still be accumulating an earlier tile's P.V (with several
             // score buffers this tile's Q.K^T was issued before it): wait
             // until every P.V so far is done.  The TMEM loads and stores are
             // warp-wide, so the warp rescales together, with alpha = 1 in rows

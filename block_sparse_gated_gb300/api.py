@@ -110,7 +110,7 @@ def _pool_strides(t: torch.Tensor, kv_layout: str):
 
 def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, softmax_scale,
             mode, thresholds, log_lambda, v_always=False, block_table=None, kv_layout="pthd",
-            mean_correction=False, schedule="paired"):
+            mean_correction=False, schedule="auto"):
     varlen = cu_seqlens is not None
     if layout is None:
         layout = "htd" if varlen else "bhld"
@@ -176,8 +176,8 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
         p.thresholds, p.thresholds_nq = None, 0
     p.log_lambda = float(log_lambda) if log_lambda is not None else 0.0
     p.dtype = _dtype_code(q)
-    if schedule not in ("paired", "pipelined"):
-        raise ValueError(f"unknown schedule {schedule!r}")
+    schedule = resolve_schedule(schedule, mode=mode, block_q=block_q, block_k=block_k,
+                                mean_correction=mean_correction)
     p.flags = (_native.FLAG_V_ALWAYS if v_always else 0) | \
         (_native.FLAG_MEAN_CORRECTION if mean_correction else 0) | \
         (_native.FLAG_PIPELINED if schedule == "pipelined" else 0)
@@ -187,6 +187,23 @@ def _params(q, k, v, o, *, layout, cu_seqlens, max_seqlen, block_q, block_k, sof
         p.page_size = page
         p.num_pages = k.shape[0]
     return p
+
+
+def resolve_schedule(schedule="auto", *, mode="threshold", block_q=128, block_k=128,
+                     mean_correction=False) -> str:
+    """The kernel schedule a call runs.  "auto" takes "pipelined" (one query
+    head per CTA, Q.K^T issued ahead of P.V by a warp of its own) for gated
+    calls with 128 x 128 blocks and no mean correction -- it is the faster
+    one there once tiles are skipped -- and "paired" (two query heads of a
+    GQA group per CTA sharing every K/V tile) for everything else."""
+    if block_k == 224:  # the 128 x 224 tile has only the one-head kernel
+        return "pipelined"
+    if schedule == "auto":
+        return ("pipelined" if mode in ("threshold", "lambda") and block_q == 128 and
+                block_k == 128 and not mean_correction else "paired")
+    if schedule not in ("paired", "pipelined"):
+        raise ValueError(f"unknown schedule {schedule!r}")
+    return schedule
 
 
 def bitmap_shape(num_heads_q: int, *, block_q: int, block_k: int, seqlens) -> tuple[int, int, int]:
@@ -202,7 +219,7 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
             thresholds=None, log_lambda=None, cu_seqlens=None, max_seqlen=None, layout=None,
             out=None, return_bitmap=False, return_lse=False, return_counts=False,
             workspace=None, stream=None, v_always=False, block_table=None, kv_layout="pthd",
-            mean_correction=False, schedule="paired"):
+            mean_correction=False, schedule="auto"):
     """Gated causal prefill.  Batched: q [B, Hq, L, d] (layout "bhld") or
     [B, L, Hq, d] ("blhd"); varlen (cu_seqlens int32 on the device): q [Hq, T, d]
     ("htd") or [T, Hq, d] ("thd").  Returns a dict with "out" and, on request,
@@ -227,8 +244,11 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
     key count (threshold and lambda modes, 128 x 128 blocks, contiguous K/V).
 
     ``schedule``: "paired" (two query heads of a GQA group per CTA, sharing
-    each K/V tile) or "pipelined" (one query head per CTA, Q.K^T of the next
-    tiles issued ahead of the current P.V; 128 x 128 blocks)."""
+    each K/V tile), "pipelined" (one query head per CTA, Q.K^T of the next
+    tiles issued ahead of the current P.V; Bq = 128, Bk = 128 or 224) or
+    "auto" (``resolve_schedule``: pipelined for gated 128 x 128 calls without
+    mean correction, else paired).  The choice never changes the bitmap or
+    the counts; outputs differ only in floating-point rounding order."""
     if out is None:
         out = torch.empty_like(q)
     dev = q.device
@@ -280,7 +300,7 @@ def prefill_workspace_bytes(q, k, v, **kw) -> int:
                 v_always=kw.get("v_always", False), block_table=kw.get("block_table"),
                 kv_layout=kw.get("kv_layout", "pthd"),
                 mean_correction=kw.get("mean_correction", False),
-                schedule=kw.get("schedule", "paired"))
+                schedule=kw.get("schedule", "auto"))
     return int(_native.lib().bsfa_prefill_workspace_size(ctypes.byref(p)))
 
 

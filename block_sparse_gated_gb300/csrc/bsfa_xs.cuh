@@ -28,7 +28,8 @@
 // Roles (384 threads, one CTA per SM, persistent over a heaviest-first list
 // of (KV head, query tile, query head) units):
 //   warp 0      TMA producer: Q per unit, K for every visible tile.
-//   warp 1      MMA issuer, TMEM owner.
+//   warp 1      P.V issuer (calibration: Q.K^T issuer), TMEM owner.
+//   warp 2      Q.K^T issuer (not calibration).
 //   warp 3      V loader: V of the tiles the gate keeps (of every tile when
 //               the gate is compiled out or with VALL).
 //   warps 4-11  softmax: warp 4 + 4 ch + wq holds, for rows 32 wq .. 32 wq
@@ -49,9 +50,10 @@ struct XsCtrl {
   uint64_t ph_full[3];   // per S buffer: P of the first half of the keys written (or skipped)
   uint64_t p_full[3];    // per S buffer: P of the second half written (or skipped)
   uint64_t dec_full[3];  // per S buffer: decision word published, 32 arrivals
-  uint64_t pv_done[2];   // per tile parity: that tile's P.V (if any) and all before it done
+  uint64_t pv_done[2];   // per kept-tile parity: that kept tile's P.V and all before it done
+  uint64_t buf_free[3];  // per S buffer: its tile is done with it (skipped, or P.V complete)
   uint64_t o_full, o_empty;
-  uint64_t drain;
+  uint64_t drain, drain_qk;
   uint32_t tmem_base;
   uint32_t dec[3];       // per S buffer: tile stamp << DEC_BITS | keep bit
   float xmax[2][2][128]; // per (tile parity, column half, row): half-row maximum
@@ -123,6 +125,10 @@ __global__ void __launch_bounds__(384, 1)
                    const __grid_constant__ CUtensorMap tmV, const DevParams p) {
   using LY = XsLayout<D, BK, CALIB>;
   constexpr int NB = LY::NB, KST = LY::KST, VST = LY::VST;
+  // Q.K^T from a warp of its own (warp 2) when there are several score
+  // buffers; with one, each Q.K^T waits for the previous tile anyway and is
+  // issued in order after its P.V by warp 1.
+  constexpr bool SPLIT = !CALIB && NB > 1;
   constexpr int VSTN = VST > 0 ? VST : 1;  // divisor for V ring indices (no V ring: unused)
   constexpr int TQ = LY::TQ, TKV = LY::TKV;
   constexpr int QHALF = TILE * 128;  // bytes of one 64-column swizzled half of Q
@@ -158,9 +164,11 @@ __global__ void __launch_bounds__(384, 1)
       c->dec[b] = 0xFFFFFFFFu;  // no stamp matches
     }
     for (int b = 0; b < 2; ++b) mbar_init(&c->pv_done[b], 1);
+    for (int b = 0; b < 3; ++b) mbar_init(&c->buf_free[b], 1);
     mbar_init(&c->o_full, 1);
     mbar_init(&c->o_empty, 256);
     mbar_init(&c->drain, 1);
+    mbar_init(&c->drain_qk, 1);
     c->abort = 0;
     fence_mbarrier_init();
   }
@@ -211,8 +219,11 @@ __global__ void __launch_bounds__(384, 1)
                               : make_int2(si.x + J * BK, si.w);
         {
           const uint32_t st = kc % KST;
-          if (!(ok = wait_all(&c->k_empty[st], ((kc / KST) & 1) ^ 1, abort, p.err,
-                              ERR_WAIT_K_EMPTY)))
+          // With as many K stages as score buffers, Q.K^T number kc reads K
+          // stage kc % KST and writes score buffer kc % NB, the same index:
+          // the stage is free once that buffer's scores are complete.
+          uint64_t* kfree = (KST == NB) ? &c->s_full[st] : &c->k_empty[st];
+          if (!(ok = wait_all(kfree, ((kc / KST) & 1) ^ 1, abort, p.err, ERR_WAIT_K_EMPTY)))
             break;
           if (elect_one()) {
             mbar_arrive_expect_tx(&c->k_full[st], TKV);
@@ -283,13 +294,18 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 1) {
-    // ----------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------- P.V issuer
     // The whole warp runs the loop and the waits; one elected lane issues
-    // every MMA and commit.  Per unit: Q.K^T of the first NB tiles, then for
-    // each tile t: its decision; if kept, P.V (P in two halves); the commit
-    // of pv_done; then Q.K^T of tile t + NB into t's score buffer (in issue
-    // order after t's P.V, which reads P from that buffer).  Calibration:
-    // the next Q.K^T follows the softmax's release of the buffer.
+    // every MMA and commit.  For each tile t: its decision; if kept, P.V (P
+    // in two halves) and the commit of pv_done.  A skipped tile needs nothing
+    // here (every access and commit of this warp queues behind the MMAs in
+    // flight).  With SPLIT, a kept tile also commits buf_free (its score
+    // buffer may take the Q.K^T of tile t + NB once that P.V is complete) and
+    // warp 2 issues every Q.K^T, as soon as a buffer is free and its K tile
+    // has landed, so a run of skipped tiles never waits for this warp.
+    // Without SPLIT (one 224-column buffer) this warp issues the Q.K^T of
+    // tile t + NB itself, in issue order after t's P.V.  Calibration: this
+    // warp issues the Q.K^T, each after the softmax's release of the buffer.
     constexpr uint32_t IDESC_QK = idesc_f32acc<F16>(128, BK, false, false);
     constexpr uint32_t IDESC_PV = idesc_f32acc<F16>(128, D, false, true);
     constexpr int KSTEPS = BK / 16, KHALFSTEPS = BK / 32;
@@ -298,6 +314,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t dV = smem_desc_sw128(smem_u32(sV), KHALF, 1024);
     const uint32_t d_o = tmem + LY::O_COL;
     uint32_t kc = 0, vc = 0, tc = 0, uc = 0;
+    uint32_t kp = 0;  // kept tiles so far (pv_done phases)
     bool ok = true;
     // Q.K^T of the unit's tile j into score buffer b.
     auto issue_s = [&](int j, int n, uint32_t b) -> bool {
@@ -308,7 +325,7 @@ __global__ void __launch_bounds__(384, 1)
       if (elect_one()) {
         xs_issue_qk<D, BK>(tmem + b * 128, dQ, dK + ((kst * TKV) >> 4), IDESC_QK);
         umma_commit(&c->s_full[b]);
-        umma_commit(&c->k_empty[kst]);
+        if constexpr (KST != NB) umma_commit(&c->k_empty[kst]);
         if (j == n - 1) umma_commit(&c->q_empty);
       }
       __syncwarp();
@@ -319,10 +336,12 @@ __global__ void __launch_bounds__(384, 1)
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
-      if (!(ok = wait_all(&c->q_full, uc & 1, abort, p.err, ERR_WAIT_Q_FULL))) break;
-      for (int j = 0; j < NB && j < n; ++j)
-        if (!(ok = issue_s(j, n, (tc + j) % NB))) break;
-      if (!ok) break;
+      if constexpr (!SPLIT) {
+        if (!(ok = wait_all(&c->q_full, uc & 1, abort, p.err, ERR_WAIT_Q_FULL))) break;
+        for (int j = 0; j < NB && j < n; ++j)
+          if (!(ok = issue_s(j, n, (tc + j) % NB))) break;
+        if (!ok) break;
+      }
       bool first = true;  // no P.V of this unit issued yet
       for (int J = 0; J < n && ok; ++J, ++tc) {
         const uint32_t b = tc % NB, ppar = (tc / NB) & 1;
@@ -334,16 +353,24 @@ __global__ void __launch_bounds__(384, 1)
           if (J + NB < n && !(ok = issue_s(J + NB, n, b))) break;
           continue;
         }
-        // Probe everything this step may need back to back (one shared-memory
-        // round trip), then block only on what is missing.  Warp-uniform: a
-        // phase counts as complete when every lane saw it so.
+        // The decision first: a skipped tile needs nothing else, and each
+        // shared-memory access of this warp (probes included) queues behind
+        // the operand reads of the MMAs in flight.  A kept tile then probes
+        // V and both halves of P back to back and blocks only on what is
+        // missing.  Warp-uniform: a phase counts as complete when every lane
+        // saw it so.
         const uint32_t vst = vc % VSTN;
-        const bool v_ok =
-            __all_sync(0xffffffffu, mbar_test_wait(&c->v_full[vst], (vc / VSTN) & 1));
-        const bool ph_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->ph_full[b], ppar));
-        const bool p_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->p_full[b], ppar));
         bool keep = true;
-        if constexpr (GATING) {
+        if constexpr (GATING && SPLIT) {
+          // Q.K^T run ahead of this warp through skipped tiles, so the word
+          // may already carry a later tile's decision: that means tile tc was
+          // skipped (a kept tile's buffer takes no later Q.K^T before this
+          // warp's P.V of it), and a reader that is behind never waits on a
+          // phase by parity alone.
+          const uint32_t w = wait_decision<NB>(&c->dec[b], &c->dec_full[b], tc, abort, p.err, &ok);
+          if (!ok) break;
+          keep = stamp_dist(w, tc) == 0 && (w & DEC_MASK) != 0u;
+        } else if constexpr (GATING) {
           // Lane 0's reading of the word, for the whole warp.
           uint32_t w = __shfl_sync(0xffffffffu, ld_acquire_u32(&c->dec[b]), 0);
           if ((w >> DEC_BITS) != (tc & DEC_STAMP_MASK)) {  // not published yet
@@ -351,6 +378,13 @@ __global__ void __launch_bounds__(384, 1)
             w = __shfl_sync(0xffffffffu, ld_acquire_u32(&c->dec[b]), 0);
           }
           keep = (w & DEC_MASK) != 0u;
+        }
+        bool v_ok = false, ph_ok = false, p_ok = false;
+        if (keep || (GATING && VALL))
+          v_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->v_full[vst], (vc / VSTN) & 1));
+        if (keep) {
+          ph_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->ph_full[b], ppar));
+          p_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->p_full[b], ppar));
         }
         const bool vload = keep || (GATING && VALL);  // this tile's V stage was filled
         if (vload && !v_ok &&
@@ -395,12 +429,18 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
         }
         if (elect_one()) {
-          umma_commit(&c->pv_done[tc & 1]);
+          if (keep) {
+            umma_commit(&c->pv_done[kp & 1]);
+            if (SPLIT) umma_commit(&c->buf_free[b]);
+          }
           if (vload) umma_commit(&c->v_empty[vst]);
         }
         __syncwarp();
+        if (keep) ++kp;
         if (vload) ++vc;
-        if (J + NB < n && !(ok = issue_s(J + NB, n, b))) break;
+        if constexpr (!SPLIT) {
+          if (J + NB < n && !(ok = issue_s(J + NB, n, b))) break;
+        }
       }
       if (!ok) break;
       if constexpr (!CALIB) {
@@ -412,6 +452,45 @@ __global__ void __launch_bounds__(384, 1)
     if (elect_one()) umma_commit(&c->drain);
     __syncwarp();
     drain_wait(&c->drain, 0);
+  } else if (SPLIT && warp == 2) {
+    // ------------------------------------------------------ Q.K^T issuer
+    // Q.K^T number g (the CTA's g-th tile, in unit order) goes into score
+    // buffer g % NB once tile g - NB is done with it (buf_free: the softmax
+    // arrives for a skip, the P.V issuer commits after a kept tile's P.V)
+    // and K tile g has landed.  Its commit on s_full also frees K stage g %
+    // KST when KST == NB.  Probes first, waits only on what is missing.
+    constexpr uint32_t IDESC_QK = idesc_f32acc<F16>(128, BK, false, false);
+    const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+    uint32_t g = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+      const int kvh = u / per_kv, rem = u - kvh * per_kv;
+      const int2 t = p.tiles[rem / p.group];
+      const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
+      if (!(ok = wait_all(&c->q_full, uc & 1, abort, p.err, ERR_WAIT_Q_FULL))) break;
+      for (int j = 0; j < n; ++j, ++g) {
+        const uint32_t b = g % NB, kst = g % KST;
+        const uint32_t fpar = ((g / NB) & 1) ^ 1, kpar = (g / KST) & 1;
+        const bool f_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->buf_free[b], fpar));
+        const bool k_ok = __all_sync(0xffffffffu, mbar_test_wait(&c->k_full[kst], kpar));
+        if (!f_ok && !(ok = wait_all(&c->buf_free[b], fpar, abort, p.err, ERR_WAIT_P_FULL)))
+          break;
+        if (!k_ok && !(ok = wait_all(&c->k_full[kst], kpar, abort, p.err, ERR_WAIT_K_FULL)))
+          break;
+        tc_fence_after();
+        if (elect_one()) {
+          xs_issue_qk<D, BK>(tmem + b * 128, dQ, dK + ((kst * TKV) >> 4), IDESC_QK);
+          umma_commit(&c->s_full[b]);
+          if constexpr (KST != NB) umma_commit(&c->k_empty[kst]);
+          if (j == n - 1) umma_commit(&c->q_empty);
+        }
+        __syncwarp();
+      }
+    }
+    if (elect_one()) umma_commit(&c->drain_qk);
+    __syncwarp();
+    drain_wait(&c->drain_qk, 0);
   } else if (warp < 4) {
     // idle
   } else {
@@ -438,7 +517,11 @@ __global__ void __launch_bounds__(384, 1)
     constexpr uint32_t NBAR = 256;
     const float sc = p.sigma_log2;
     const bool lambda_mode = GATING && !CALIB && p.mode == 1;
+    // ln(lambda) = -inf keeps every block: no running max to keep exact, so
+    // no exchange of half-row maxima for it.
+    const bool lambda_vote = lambda_mode && p.log_lambda != -CUDART_INF_F;
     uint32_t tc = 0, uc = 0;
+    uint32_t kn = 0;  // kept tiles so far (pv_done phases)
     bool ok = true;
     uint32_t cnt_kept = 0, cnt_cand = 0, cnt_diag = 0;
 
@@ -529,7 +612,7 @@ __global__ void __launch_bounds__(384, 1)
           else want = rvalid && (lm - m_true) * p.sigma >= p.log_lambda;
         }
         const bool need_x =
-            rvalid && (((lm - m_used) * sc > RESCALE_LOG2) || (lambda_mode && lm > m_true));
+            rvalid && (((lm - m_used) * sc > RESCALE_LOG2) || (lambda_vote && lm > m_true));
         // Every read of S is complete (tcgen05.wait::ld above); the fence
         // orders it before the barrier, after which the MMA warp may refill a
         // skipped tile's buffer and the other half's P may overwrite my
@@ -553,6 +636,10 @@ __global__ void __launch_bounds__(384, 1)
         if (GATING && lead_warp) {  // all 32 lanes: same value, 32 arrivals
           st_release_u32(&c->dec[b], ((tc & DEC_STAMP_MASK) << DEC_BITS) | (kept ? 1u : 0u));
           mbar_arrive(&c->dec_full[b]);
+          // A skipped tile's buffer is free: every read of its scores was
+          // fenced before the barrier above.
+          if (SPLIT && !kept && elect_one()) mbar_arrive(&c->buf_free[b]);
+          __syncwarp();
         }
 
         // ---- online softmax over my half of a kept tile
@@ -573,7 +660,7 @@ __global__ void __launch_bounds__(384, 1)
             // that keep their reference.  A wait that gives up raises the
             // abort flag, which the next tile barrier turns into a common exit.
             if (o_init && __any_sync(0xffffffffu, resc)) {
-              wait_bar(&c->pv_done[(tc - 1) & 1], ((tc - 1) >> 1) & 1, abort, p.err,
+              wait_bar(&c->pv_done[(kn - 1) & 1], ((kn - 1) >> 1) & 1, abort, p.err,
                        ERR_WAIT_O_FULL);
               __syncwarp();
               tc_fence_after();
@@ -642,6 +729,7 @@ __global__ void __launch_bounds__(384, 1)
           l += ls0 + ls1;
           tmem_wait_st();
           o_init = true;
+          ++kn;
         }
         // My half of P is written (or the tile skipped): one arrival per
         // thread and tile on this half's barrier (first half: ph_full).

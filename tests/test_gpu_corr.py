@@ -107,7 +107,8 @@ def test_correction_without_skips_changes_nothing(cuda_device):
     x = wl.layer_inputs(Hq, Hkv, L, d, 440)
     q, k, v = (t.to(cuda_device)[None] for t in (x.q, x.k, x.v))
     T = torch.full((Hq, 1), -math.inf, device=cuda_device)
-    a = _run(q, k, v, mode="threshold", thresholds=T)
+    # Mean correction runs in the paired kernel: compare within it.
+    a = _run(q, k, v, mode="threshold", thresholds=T, schedule="paired")
     b = _run(q, k, v, mode="threshold", thresholds=T, mean_correction=True)
     for key in ("out", "lse", "bitmap", "counts"):
         assert torch.equal(a[key], b[key]), key

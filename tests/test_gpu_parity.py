@@ -28,6 +28,16 @@ def _inputs(Hq, Hkv, L, d, seed, dev, **kw):
     return x, x.q.to(dev), x.k.to(dev), x.v.to(dev)
 
 
+# Gated 128 x 128 calls run the one-head kernel by default ("auto"); the
+# cases below that take `schedule` also run the paired kernel explicitly.
+SCHEDULES = ["auto", "paired"]
+
+
+def _skip_redundant(schedule, Bq=128, Bk=128):
+    if schedule == "paired" and (Bq, Bk) != (128, 128):
+        pytest.skip("auto already runs the paired kernel for these block sizes")
+
+
 def _run(q, k, v, **kw):
     b = _bsfa()
     r = b.prefill(q[None], k[None], v[None], return_bitmap=True, return_lse=True,
@@ -64,14 +74,15 @@ def test_zero_queries_average_values(cuda_device):
 
 
 # ------------------------------------------------------------ threshold gate
-def _threshold_case(dev, Hq, Hkv, L, d, Bq, Bk, seed, table, needles=0, sink=0):
+def _threshold_case(dev, Hq, Hkv, L, d, Bq, Bk, seed, table, needles=0, sink=0,
+                    schedule="auto"):
     x, q, k, v = _inputs(Hq, Hkv, L, d, seed, dev, needles=needles, sink_tokens=sink,
                          block=max(Bq, Bk))
     q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
     sigma = gu.default_sigma(d)
     T, n_adj, _ = gu.guarded_thresholds(q64, k64, table, Bq, Bk, sigma)
     r = _run(q, k, v, block_q=Bq, block_k=Bk, mode="threshold",
-             thresholds=torch.from_numpy(T).to(dev))
+             thresholds=torch.from_numpy(T).to(dev), schedule=schedule)
     ref = orc.prefill(q64, k64, v64, Bq=Bq, Bk=Bk, thresholds=T.astype(np.float64))
     bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, [L], Bq, Bk)
     assert clean
@@ -88,12 +99,15 @@ def _threshold_case(dev, Hq, Hkv, L, d, Bq, Bk, seed, table, needles=0, sink=0):
     return ref
 
 
+@pytest.mark.parametrize("schedule", SCHEDULES)
 @pytest.mark.parametrize("Bq,Bk", [(128, 128), (64, 64), (128, 64), (64, 128)])
 @pytest.mark.parametrize("Hq,Hkv,L,d", [(4, 2, 1000, 128), (2, 2, 700, 64), (4, 1, 513, 128)])
-def test_threshold_gate_matches_oracle(cuda_device, Bq, Bk, Hq, Hkv, L, d):
+def test_threshold_gate_matches_oracle(cuda_device, Bq, Bk, Hq, Hkv, L, d, schedule):
+    _skip_redundant(schedule, Bq, Bk)
     x = wl.layer_inputs(Hq, Hkv, L, d, 21, needles=2, block=max(Bq, Bk))
     table = gu.median_table(gu.to64(x.q), gu.to64(x.k), Bq, Bk, gu.default_sigma(d))
-    ref = _threshold_case(cuda_device, Hq, Hkv, L, d, Bq, Bk, 21, table, needles=2)
+    ref = _threshold_case(cuda_device, Hq, Hkv, L, d, Bq, Bk, 21, table, needles=2,
+                          schedule=schedule)
     cand = ref["candidate"]
     kept = (ref["keep"] & cand).sum()
     assert 0 < kept < cand.sum()  # the case really gates
@@ -129,15 +143,17 @@ def test_tiny_workload_calibrated(cuda_device):
 
 
 # ---------------------------------------------------------------- lambda gate
+@pytest.mark.parametrize("schedule", SCHEDULES)
 @pytest.mark.parametrize("Bq,Bk,skip_rate", [(128, 128, 0.5), (64, 64, 0.5), (128, 64, 0.5),
                                              (64, 128, 0.5), (128, 128, 0.0)])
-def test_lambda_gate_matches_oracle(cuda_device, Bq, Bk, skip_rate):
+def test_lambda_gate_matches_oracle(cuda_device, Bq, Bk, skip_rate, schedule):
+    _skip_redundant(schedule, Bq, Bk)
     Hq, Hkv, L, d = 4, 2, 1500, 128
     x, q, k, v = _inputs(Hq, Hkv, L, d, 31, cuda_device, skip_rate=skip_rate, block=Bk)
     q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
     sigma = gu.default_sigma(d)
     ll = gu.guarded_log_lambda(-1.0 if skip_rate > 0 else -1e30, Bq, Bk, sigma, [(q64, k64)])
-    r = _run(q, k, v, block_q=Bq, block_k=Bk, mode="lambda", log_lambda=ll)
+    r = _run(q, k, v, block_q=Bq, block_k=Bk, mode="lambda", log_lambda=ll, schedule=schedule)
     ref = orc.prefill(q64, k64, v64, Bq=Bq, Bk=Bk, mode="lambda", log_lambda=ll)
     bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, [L], Bq, Bk)
     assert clean
@@ -149,8 +165,11 @@ def test_lambda_gate_matches_oracle(cuda_device, Bq, Bk, skip_rate):
 
 
 # ---------------------------------------------------------------- varlen
+@pytest.mark.parametrize("schedule", SCHEDULES)
 @pytest.mark.parametrize("mode", ["threshold", "lambda", "none"])
-def test_varlen_matches_oracle(cuda_device, mode):
+def test_varlen_matches_oracle(cuda_device, mode, schedule):
+    if schedule == "paired" and mode == "none":
+        pytest.skip("auto already runs the paired kernel with the gate compiled out")
     Hq, Hkv, d, B = 4, 2, 128, 128
     lens = [100, 0, 300, 129, 640, 1]
     parts = [wl.layer_inputs(Hq, Hkv, Ln, d, 40 + n, skip_rate=0.4) if Ln else None
@@ -180,7 +199,7 @@ def test_varlen_matches_oracle(cuda_device, mode):
     b = _bsfa()
     r = b.prefill(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
                   cu_seqlens=cu.to(cuda_device), max_seqlen=max(lens), mode=mode,
-                  return_bitmap=True, return_lse=True, **kw)
+                  return_bitmap=True, return_lse=True, schedule=schedule, **kw)
     torch.cuda.synchronize()
     assert b.api.device_error() == 0
     okw = dict(mode={"none": "dense"}.get(mode, mode))
@@ -261,15 +280,17 @@ def test_soak_back_to_back_launches(cuda_device):
 
 
 # ------------------------------------------------------- V loaded for every tile
+@pytest.mark.parametrize("schedule", SCHEDULES)
 @pytest.mark.parametrize("mode", ["threshold", "lambda"])
 @pytest.mark.parametrize("Bq,Bk,d", [(128, 128, 128), (64, 64, 64)])
-def test_v_always_is_bit_identical(cuda_device, mode, Bq, Bk, d):
+def test_v_always_is_bit_identical(cuda_device, mode, Bq, Bk, d, schedule):
+    _skip_redundant(schedule, Bq, Bk)
     """Loading V for skipped tiles too (the flag that exists for the A/B
     against skipping the load) changes no output bit; the case does skip
     blocks."""
     Hq, Hkv, L = 4, 2, 1500
     x, q, k, v = _inputs(Hq, Hkv, L, d, 91, cuda_device, skip_rate=0.6, needles=2, block=Bk)
-    kw = dict(block_q=Bq, block_k=Bk, mode=mode)
+    kw = dict(block_q=Bq, block_k=Bk, mode=mode, schedule=schedule)
     if mode == "lambda":
         kw["log_lambda"] = -1.0
     else:
@@ -285,15 +306,18 @@ def test_v_always_is_bit_identical(cuda_device, mode, Bq, Bk, d):
 
 
 # ------------------------------------------------- gates that keep everything
-def test_keep_all_gate_with_and_without_vote(cuda_device):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_keep_all_gate_with_and_without_vote(cuda_device, schedule):
     """A -inf threshold row (or ln(lambda) = -inf) keeps every block without
-    a vote; -1e30 keeps every block after one.  Both give the same bytes."""
+    a vote (paired kernel) or without keeping an exact running max (one-head
+    kernel); -1e30 keeps every block after a vote.  All give the same bytes."""
     Hq, Hkv, L, d = 4, 2, 1000, 128
     x, q, k, v = _inputs(Hq, Hkv, L, d, 95, cuda_device, skip_rate=0.5)
-    a = _run(q, k, v, mode="threshold", thresholds=torch.full((Hq, 1), -math.inf, device=cuda_device))
-    b = _run(q, k, v, mode="threshold", thresholds=torch.full((Hq, 1), -1e30, device=cuda_device))
-    c = _run(q, k, v, mode="lambda", log_lambda=-math.inf)
-    d_ = _run(q, k, v, mode="lambda", log_lambda=-1e30)
+    s = dict(schedule=schedule)
+    a = _run(q, k, v, mode="threshold", thresholds=torch.full((Hq, 1), -math.inf, device=cuda_device), **s)
+    b = _run(q, k, v, mode="threshold", thresholds=torch.full((Hq, 1), -1e30, device=cuda_device), **s)
+    c = _run(q, k, v, mode="lambda", log_lambda=-math.inf, **s)
+    d_ = _run(q, k, v, mode="lambda", log_lambda=-1e30, **s)
     for r in (b, c, d_):
         for key in ("out", "lse", "bitmap", "counts"):
             assert torch.equal(a[key], r[key]), key
@@ -301,7 +325,8 @@ def test_keep_all_gate_with_and_without_vote(cuda_device):
     assert kept == cand
 
 
-def test_mixed_trivial_and_voting_units(cuda_device):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_mixed_trivial_and_voting_units(cuda_device, schedule):
     """Within one call, units whose threshold entries are all -inf (no vote)
     next to units that vote, including the two query heads of one CTA (a
     GQA pair) taking different paths: against the oracle."""
@@ -311,12 +336,14 @@ def test_mixed_trivial_and_voting_units(cuda_device):
     table[0, ::2] = -np.inf        # head 0: every other query block without a vote
     table[2, :] = -np.inf          # head 2: all -inf, its pair partner (head 3) votes
     table[1, 5:] = -np.inf         # head 1: -inf from query block 5 on
-    ref = _threshold_case(cuda_device, Hq, Hkv, L, d, 128, 128, 96, table, needles=2)
+    ref = _threshold_case(cuda_device, Hq, Hkv, L, d, 128, 128, 96, table, needles=2,
+                          schedule=schedule)
     cand = ref["candidate"]
     assert (ref["keep"][3] & cand[3]).sum() < cand[3].sum()  # head 3 really gates
 
 
-def test_high_skip_soak_many_units_per_cta(cuda_device):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_high_skip_soak_many_units_per_cta(cuda_device, schedule):
     """About 94% of the candidates skipped, query blocks below the budget at
     -inf (kept without a vote), many units per CTA, 20 back-to-back calls:
     no bounded wait may run out (a softmax running through skipped tiles
@@ -340,14 +367,14 @@ def test_high_skip_soak_many_units_per_cta(cuda_device):
     T[:, kb:] = np.where(np.isfinite(T[:, kb:]), T[:, kb:], fill)
     Td = torch.from_numpy(T).to(cuda_device)
     first = b.prefill(q[None], k[None], v[None], mode="threshold", thresholds=Td,
-                      return_bitmap=True, return_counts=True)
+                      return_bitmap=True, return_counts=True, schedule=schedule)
     torch.cuda.synchronize()
     assert b.api.device_error() == 0
     kept, cand = first["counts"].cpu().tolist()[:2]
     assert 1 - kept / cand > 0.85
     for _ in range(20):
         r = b.prefill(q[None], k[None], v[None], mode="threshold", thresholds=Td,
-                      return_bitmap=True)
+                      return_bitmap=True, schedule=schedule)
         torch.cuda.synchronize()
         assert b.api.device_error() == 0
         assert torch.equal(r["out"], first["out"])

@@ -73,7 +73,7 @@ def test_pipelined_matches_oracle(cuda_device, mode, Hq, Hkv, L, d, dtype):
     if mode != "none":
         assert 0 < cnt[0] < cnt[1]  # the case really gates
         # The paired schedule takes the same decisions.
-        rp = _run(q, k, v, mode=mode, **kw)
+        rp = _run(q, k, v, mode=mode, schedule="paired", **kw)
         assert torch.equal(rp["bitmap"], r["bitmap"])
         assert torch.equal(rp["counts"], r["counts"])
 

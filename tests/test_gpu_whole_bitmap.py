@@ -60,7 +60,7 @@ def _layer(dev, name, seed_rep=0, **kw):
     return cfg, x
 
 
-def _threshold_whole(dev, cfg, x, smax, heads, k):
+def _threshold_whole(dev, cfg, x, smax, heads, k, schedule="auto"):
     Hq, Hkv, L, B = cfg["Hq"], cfg["Hkv"], cfg["L"], cfg["Bk"]
     nq = orc.num_blocks(L, B)
     rows = {}
@@ -71,7 +71,7 @@ def _threshold_whole(dev, cfg, x, smax, heads, k):
     T = _budget_table(rows, Hq, nq, k, fill)
     r = bsfa.prefill(x.q[None], x.k[None], x.v[None], block_q=B, block_k=B, mode="threshold",
                      thresholds=torch.from_numpy(T).to(dev), return_bitmap=True,
-                     return_counts=True)
+                     return_counts=True, schedule=schedule)
     torch.cuda.synchronize()
     assert bsfa.api.device_error() == 0
     bits = _gpu_bits(r, Hq, [L], B)[0]
@@ -86,14 +86,24 @@ def _threshold_whole(dev, cfg, x, smax, heads, k):
     return r, kept, cand
 
 
-def test_llama_32k_whole_bitmap_all_heads(cuda_device):
-    """The 32K layer, every head and query block, budget k = 64 per row."""
+@pytest.fixture(scope="module")
+def llama_32k(cuda_device):
     cfg, x = _layer(cuda_device, "llama8b-L32768")
     Hq, g, d, B = cfg["Hq"], cfg["Hq"] // cfg["Hkv"], cfg["d"], cfg["Bk"]
     sigma = 1.0 / math.sqrt(d)
     smax = {h: orc.block_maxima(gu.to64(x.q[h]), gu.to64(x.k[h // g]), B, B, sigma)
             for h in range(Hq)}
-    r, kept, cand = _threshold_whole(cuda_device, cfg, x, smax, range(Hq), cfg["ks"][0])
+    return cfg, x, smax
+
+
+@pytest.mark.parametrize("schedule", ["auto", "paired"])
+def test_llama_32k_whole_bitmap_all_heads(cuda_device, llama_32k, schedule):
+    """The 32K layer, every head and query block, budget k = 64 per row, in
+    the default (one-head) and the paired schedule."""
+    cfg, x, smax = llama_32k
+    Hq, B = cfg["Hq"], cfg["Bk"]
+    r, kept, cand = _threshold_whole(cuda_device, cfg, x, smax, range(Hq), cfg["ks"][0],
+                                     schedule=schedule)
     kc, cc, diag = r["counts"].cpu().tolist()
     assert (kc, cc) == (kept, cand)
     assert diag == Hq * orc.num_blocks(cfg["L"], B)

@@ -256,11 +256,14 @@ __global__ void __launch_bounds__(384, 1)
       const int2 t = p.tiles[rem / p.group];
       const int4 si = p.seqinfo[t.x];
       const int n = xs_ntiles<BK>(t.y, si.y);
+      // A unit whose gate keeps everything needs every V without reading the
+      // decisions (they are still published; the reads go by stamp).
+      const bool triv = GATING && unit_gate_trivial(p, kvh * p.group + rem % p.group, t.y);
       for (int J = 0; J < n; ++J, ++tc) {
         const int2 cc = PAGED ? kv_tile_coord<PAGED>(p, si, t.x, J)
                               : make_int2(si.x + J * BK, si.w);  // before the waits
-        bool need = VALL || !GATING;
-        if constexpr (GATING && !VALL) {
+        bool need = VALL || !GATING || triv;
+        if (GATING && !VALL && !triv) {
           // The decision word of the tile's S buffer carries the tile stamp.  A
           // word stamped with a later tile also means a skip: a kept tile's
           // P.V waits for its V, and the next Q.K^T into that buffer (whose
@@ -336,6 +339,9 @@ __global__ void __launch_bounds__(384, 1)
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
+      // A unit whose gate keeps everything: no decision to read (the softmax
+      // still publishes them, so the phases stay one per tile).
+      const bool triv = GATING && !CALIB && unit_gate_trivial(p, kvh * p.group + rem % p.group, t.y);
       if constexpr (!SPLIT) {
         if (!(ok = wait_all(&c->q_full, uc & 1, abort, p.err, ERR_WAIT_Q_FULL))) break;
         for (int j = 0; j < NB && j < n; ++j)
@@ -361,7 +367,9 @@ __global__ void __launch_bounds__(384, 1)
         // saw it so.
         const uint32_t vst = vc % VSTN;
         bool keep = true;
-        if constexpr (GATING && SPLIT) {
+        if (triv) {
+          // keep
+        } else if constexpr (GATING && SPLIT) {
           // Q.K^T run ahead of this warp through skipped tiles, so the word
           // may already carry a later tile's decision: that means tile tc was
           // skipped (a kept tile's buffer takes no later Q.K^T before this
@@ -611,8 +619,14 @@ __global__ void __launch_bounds__(384, 1)
           if (!lambda_mode) want = rvalid && lm * p.sigma >= tq;
           else want = rvalid && (lm - m_true) * p.sigma >= p.log_lambda;
         }
-        const bool need_x =
-            rvalid && (((lm - m_used) * sc > RESCALE_LOG2) || (lambda_vote && lm > m_true));
+        // With a lambda vote every tile exchanges the half-row maxima (written
+        // before the tile barrier, read after it): the vote needs the exact
+        // running max whenever it rises, and a second barrier for each rise
+        // costs more than the two shared-memory accesses.  Otherwise the
+        // exchange happens only when some row needs it (a rise of the lazily
+        // rescaled reference).
+        if (lambda_vote) c->xmax[tc & 1][ch][row] = lm;
+        const bool need_x = rvalid && !lambda_vote && (lm - m_used) * sc > RESCALE_LOG2;
         // Every read of S is complete (tcgen05.wait::ld above); the fence
         // orders it before the barrier, after which the MMA warp may refill a
         // skipped tile's buffer and the other half's P may overwrite my
@@ -626,12 +640,13 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t nv = bar_red_popc(bar_id, NBAR, lane == 0 ? wx : (lane <= 16 && wv));
         const bool kept = !GATING || !cand || nv >= 16u;
         float rowmax = lm;  // the row's maximum over both halves (exact when exchanged)
-        if ((nv & 15u) != 0u) {
-          c->xmax[tc & 1][ch][row] = lm;
+        const bool exact = lambda_vote || (nv & 15u) != 0u;
+        if ((nv & 15u) != 0u) {  // an exchange, or a thread that stopped
+          if (!lambda_vote) c->xmax[tc & 1][ch][row] = lm;
           ok = bar_red_and(bar_id, NBAR, okl);
           if (!ok) break;
-          rowmax = fmaxf(lm, c->xmax[tc & 1][ch ^ 1][row]);
         }
+        if (exact) rowmax = fmaxf(lm, c->xmax[tc & 1][ch ^ 1][row]);
         if (lambda_mode && kept) m_true = fmaxf(m_true, rowmax);
         if (GATING && lead_warp) {  // all 32 lanes: same value, 32 arrivals
           st_release_u32(&c->dec[b], ((tc & DEC_STAMP_MASK) << DEC_BITS) | (kept ? 1u : 0u));
@@ -644,7 +659,7 @@ __global__ void __launch_bounds__(384, 1)
 
         // ---- online softmax over my half of a kept tile
         if (kept) {
-          if ((nv & 15u) != 0u) {  // rowmax is exact: rescale when the reference must rise
+          if (exact) {  // rowmax is exact: rescale when the reference must rise
             const float m_new = fmaxf(m_used, rowmax);
             const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
             float alpha = 1.f;

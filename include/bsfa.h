@@ -118,10 +118,13 @@ typedef enum {
    * as soon as tile t's decision (a skip) or P (a keep) is in, ahead of its
    * P.V ("Skipping attention blocks was the easy part", section "Cross-stage
    * P").  Requires block_q == 128, block_k == 128 or 224, and no mean
-   * correction, else BSFA_ERR_UNSUPPORTED.  Exists as a measured alternative
-   * schedule.  The 128 x 224 tile always runs one query head per CTA (its
-   * 224-column score buffer fits TMEM once, not twice), with or without this
-   * flag. */
+   * correction, else BSFA_ERR_UNSUPPORTED.  With three score buffers and the
+   * Q.K^T issued by a warp of its own, it is the faster schedule for gated
+   * calls (threshold or lambda) with 128 x 128 blocks once tiles are
+   * skipped (the Python binding's default picks it there); the paired
+   * schedule is faster with the gate compiled out.  The 128 x 224 tile
+   * always runs one query head per CTA (its 224-column score buffer fits
+   * TMEM once, not twice), with or without this flag. */
   BSFA_FLAG_PIPELINED = 4
 } bsfa_flag;
 

@@ -602,6 +602,16 @@ def lambda_sweep(dev, args):
                 "lambda": ovh("ms_lambda_minus_inf"),
                 "note": "a -inf threshold row (calibration gives one to query blocks with fewer "
                         "than k candidates) or ln(lambda) = -inf keeps every block"},
+            # Against the same (default, one-head) kernel with the gate compiled out.
+            "zero_skip_overhead_same_kernel": {
+                "gate_compiled_out_ms": r0["ms_gate_compiled_out_pipelined"],
+                "threshold": round(r0["ms_threshold_keep_all"] /
+                                   r0["ms_gate_compiled_out_pipelined"] - 1, 4),
+                "lambda": round(r0["ms"] / r0["ms_gate_compiled_out_pipelined"] - 1, 4),
+                "threshold_minus_inf": round(r0["ms_threshold_minus_inf"] /
+                                             r0["ms_gate_compiled_out_pipelined"] - 1, 4),
+                "lambda_minus_inf": round(r0["ms_lambda_minus_inf"] /
+                                          r0["ms_gate_compiled_out_pipelined"] - 1, 4)},
             "zero_skip_overhead_paired": {
                 "lambda": round(r0["ms_paired"] / base - 1, 4),
                 "threshold": ovh("ms_threshold_keep_all_paired"),

@@ -552,6 +552,7 @@ __global__ void __launch_bounds__(384, 1)
       // this half's share of the normaliser.
       float m_used = -CUDART_INF_F, m_true = -CUDART_INF_F, l = 0.f;
       bool o_init = false;
+      bool prev_kept = false;  // lambda vote: the unit's previous tile was kept
       uint32_t bm_word = 0;
 
       for (int J = 0; J < n; ++J, ++tc) {
@@ -576,6 +577,11 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int q = 0; q < NCH; ++q) tmem_ld32_max(tS + q * 32, sr[q], qm[q]);
           if constexpr (TAIL > 0) tmem_ld16(tS + NCH * 32, stl);
+          // Lambda vote: the other half's maximum of the previous (kept) tile,
+          // stored before that tile's barrier, joins the running max here,
+          // while the TMEM loads are in flight.
+          if (lambda_vote && prev_kept)
+            m_true = fmaxf(m_true, c->xmax[(tc - 1) & 1][ch ^ 1][row]);
           tmem_wait_ld();
           if (cand) {
 #pragma unroll
@@ -619,14 +625,13 @@ __global__ void __launch_bounds__(384, 1)
           if (!lambda_mode) want = rvalid && lm * p.sigma >= tq;
           else want = rvalid && (lm - m_true) * p.sigma >= p.log_lambda;
         }
-        // With a lambda vote every tile exchanges the half-row maxima (written
-        // before the tile barrier, read after it): the vote needs the exact
-        // running max whenever it rises, and a second barrier for each rise
-        // costs more than the two shared-memory accesses.  Otherwise the
-        // exchange happens only when some row needs it (a rise of the lazily
-        // rescaled reference).
+        // With a lambda vote each half stores its maximum before the tile
+        // barrier, every tile; the other half folds it into its running max
+        // at the next tile (above), which is the first vote that needs it.
+        // The exchange after the barrier happens only when some row needs the
+        // exact maximum now (a rise of the lazily rescaled reference).
         if (lambda_vote) c->xmax[tc & 1][ch][row] = lm;
-        const bool need_x = rvalid && !lambda_vote && (lm - m_used) * sc > RESCALE_LOG2;
+        const bool need_x = rvalid && (lm - m_used) * sc > RESCALE_LOG2;
         // Every read of S is complete (tcgen05.wait::ld above); the fence
         // orders it before the barrier, after which the MMA warp may refill a
         // skipped tile's buffer and the other half's P may overwrite my
@@ -640,7 +645,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t nv = bar_red_popc(bar_id, NBAR, lane == 0 ? wx : (lane <= 16 && wv));
         const bool kept = !GATING || !cand || nv >= 16u;
         float rowmax = lm;  // the row's maximum over both halves (exact when exchanged)
-        const bool exact = lambda_vote || (nv & 15u) != 0u;
+        const bool exact = (nv & 15u) != 0u;
         if ((nv & 15u) != 0u) {  // an exchange, or a thread that stopped
           if (!lambda_vote) c->xmax[tc & 1][ch][row] = lm;
           ok = bar_red_and(bar_id, NBAR, okl);
@@ -648,6 +653,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (exact) rowmax = fmaxf(lm, c->xmax[tc & 1][ch ^ 1][row]);
         if (lambda_mode && kept) m_true = fmaxf(m_true, rowmax);
+        prev_kept = kept;
         if (GATING && lead_warp) {  // all 32 lanes: same value, 32 arrivals
           st_release_u32(&c->dec[b], ((tc & DEC_STAMP_MASK) << DEC_BITS) | (kept ? 1u : 0u));
           mbar_arrive(&c->dec_full[b]);

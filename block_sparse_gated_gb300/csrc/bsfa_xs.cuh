@@ -256,14 +256,14 @@ __global__ void __launch_bounds__(384, 1)
       const int2 t = p.tiles[rem / p.group];
       const int4 si = p.seqinfo[t.x];
       const int n = xs_ntiles<BK>(t.y, si.y);
-      // A unit whose gate keeps everything needs every V without reading the
-      // decisions (they are still published; the reads go by stamp).
-      const bool triv = GATING && unit_gate_trivial(p, kvh * p.group + rem % p.group, t.y);
       for (int J = 0; J < n; ++J, ++tc) {
         const int2 cc = PAGED ? kv_tile_coord<PAGED>(p, si, t.x, J)
                               : make_int2(si.x + J * BK, si.w);  // before the waits
-        bool need = VALL || !GATING || triv;
-        if (GATING && !VALL && !triv) {
+        // Also in a unit whose gate keeps everything, V waits for each
+        // published decision: issued as early as a stage is free (as with
+        // VALL), the V copies delay the K copies the Q.K^T issuer waits on.
+        bool need = VALL || !GATING;
+        if constexpr (GATING && !VALL) {
           // The decision word of the tile's S buffer carries the tile stamp.  A
           // word stamped with a later tile also means a skip: a kept tile's
           // P.V waits for its V, and the next Q.K^T into that buffer (whose

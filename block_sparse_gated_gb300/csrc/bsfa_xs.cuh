@@ -2,12 +2,14 @@
 // CTA, one 128-row query tile per unit, key tiles of BK = 128 or 224 keys,
 // each key tile one semantic block (Bq = 128, Bk = BK).
 //
-// BK = 128, the pipelined schedule: the scores of key tiles t, t+1 and t+2
-// live in three TMEM buffers, so Q.K^T of tile t+3 is issued as soon as tile
-// t's gate decision (a skip) or its P (a keep) is in ("Skipping attention
-// blocks was the easy part", section "Cross-stage P": the next tile's Q.K^T
-// does not wait for the current tile's P.V).  Two tiles' Q.K^T then run
-// while a third is being decided, which is what a run of skipped tiles needs.
+// BK = 128, the pipelined schedule (the default for gated 128 x 128 calls):
+// the scores of key tiles t, t+1 and t+2 live in three TMEM buffers, and a
+// warp of its own issues Q.K^T of tile t+3 as soon as tile t is done with its
+// buffer -- skipped (the softmax frees it right after the vote) or its P.V
+// complete ("Skipping attention blocks was the easy part", section
+// "Cross-stage P": the next tile's Q.K^T does not wait for the current
+// tile's P.V).  Two tiles' Q.K^T then run while a third is being decided,
+// which is what a run of skipped tiles needs.
 //
 // BK = 224, the H100 deployment tile of "Block Sparse Flash Attention"
 // ("Loss & Training": a 128-row query tile and a 224-key tile): one 224-column
@@ -49,7 +51,7 @@ struct XsCtrl {
   uint64_t s_full[3];    // per S buffer: scores of its current tile ready
   uint64_t ph_full[3];   // per S buffer: P of the first half of the keys written (or skipped)
   uint64_t p_full[3];    // per S buffer: P of the second half written (or skipped)
-  uint64_t dec_full[3];  // per S buffer: decision word published, 32 arrivals
+  uint64_t dec_full[3];  // per S buffer: decision word published (32 arrivals, one warp)
   uint64_t pv_done[2];   // per kept-tile parity: that kept tile's P.V and all before it done
   uint64_t buf_free[3];  // per S buffer: its tile is done with it (skipped, or P.V complete)
   uint64_t o_full, o_empty;

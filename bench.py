@@ -420,33 +420,36 @@ def paged_leg(q, k, v, slices, ks, outs, Bq, Bk, dev, page=256, reps=3):
 def mean_correction_leg(q, k, v, slices, ks, Bq, Bk, dev, reps=3):
     """Cost of the mean-correction option on the k=128 slice: the same gate
     (identical bitmap), plus the block-mean pass and one correction tile per
-    128 candidate blocks of every query tile.  Mean correction runs in the
-    paired kernel, so the plain call it is timed against does too; the
-    default (one-head) schedule's time for the same call is reported
-    beside it."""
+    128 candidate blocks of every query tile.  Both kernels carry the option;
+    each is timed with and without it, and "default" names the one that
+    schedule="auto" takes for a corrected call."""
     import torch
 
     import block_sparse_gated_gb300 as bsfa
     i = ks.index(128) if 128 in ks else 0
     out = torch.empty_like(q)
-    kw = dict(block_q=Bq, block_k=Bk, mode="threshold", thresholds=slices[i], out=out,
-              schedule="paired")
+    kw = dict(block_q=Bq, block_k=Bk, mode="threshold", thresholds=slices[i], out=out)
     need = bsfa.api.prefill_workspace_bytes(q, k, v, mean_correction=True, **kw)
     ws = torch.empty(need, dtype=torch.uint8, device=dev)
-    a = bsfa.prefill(q, k, v, return_bitmap=True, workspace=ws, **kw)["bitmap"].clone()
-    b = bsfa.prefill(q, k, v, return_bitmap=True, workspace=ws, mean_correction=True,
-                     **kw)["bitmap"]
-    torch.cuda.synchronize()
-    ms_plain = _timed(lambda: bsfa.prefill(q, k, v, workspace=ws, **kw), reps)
-    ms_corr = _timed(lambda: bsfa.prefill(q, k, v, workspace=ws, mean_correction=True, **kw),
-                     reps)
-    kw["schedule"] = "auto"
-    ms_default = _timed(lambda: bsfa.prefill(q, k, v, workspace=ws, **kw), reps)
-    return {"k": ks[i], "ms_plain": round(ms_plain, 3), "ms_corrected": round(ms_corr, 3),
-            "ms_default_schedule": round(ms_default, 3),
-            "corrected_over_plain": round(ms_corr / ms_plain, 4),
-            "bitmap_identical": bool(torch.equal(a, b)),
-            "workspace_bytes": int(need)}
+    res = {"k": ks[i],
+           "default": bsfa.api.resolve_schedule("auto", mode="threshold", block_q=Bq,
+                                                block_k=Bk, mean_correction=True),
+           "workspace_bytes": int(need)}
+    for sched in ("pipelined", "paired"):
+        kw["schedule"] = sched
+        a = bsfa.prefill(q, k, v, return_bitmap=True, workspace=ws, **kw)["bitmap"].clone()
+        b = bsfa.prefill(q, k, v, return_bitmap=True, workspace=ws, mean_correction=True,
+                         **kw)["bitmap"]
+        torch.cuda.synchronize()
+        same = bool(torch.equal(a, b))
+        del a, b
+        ms_plain = _timed(lambda: bsfa.prefill(q, k, v, workspace=ws, **kw), reps)
+        ms_corr = _timed(lambda: bsfa.prefill(q, k, v, workspace=ws, mean_correction=True,
+                                              **kw), reps)
+        res[sched] = {"ms_plain": round(ms_plain, 3), "ms_corrected": round(ms_corr, 3),
+                      "corrected_over_plain": round(ms_corr / ms_plain, 4),
+                      "bitmap_identical": same}
+    return res
 
 
 def e2e(q, k, v, slices, flops, Bq, Bk, args, dev):

@@ -193,14 +193,15 @@ def resolve_schedule(schedule="auto", *, mode="threshold", block_q=128, block_k=
                      mean_correction=False) -> str:
     """The kernel schedule a call runs.  "auto" takes "pipelined" (one query
     head per CTA, Q.K^T issued ahead of P.V by a warp of its own) for gated
-    calls with 128 x 128 blocks and no mean correction -- it is the faster
-    one there once tiles are skipped -- and "paired" (two query heads of a
-    GQA group per CTA sharing every K/V tile) for everything else."""
+    calls with 128 x 128 blocks, with or without mean correction -- it is the
+    faster one there once tiles are skipped -- and "paired" (two query heads
+    of a GQA group per CTA sharing every K/V tile) for everything else."""
+    del mean_correction  # both kernels carry it; the choice does not depend on it
     if block_k == 224:  # the 128 x 224 tile has only the one-head kernel
         return "pipelined"
     if schedule == "auto":
         return ("pipelined" if mode in ("threshold", "lambda") and block_q == 128 and
-                block_k == 128 and not mean_correction else "paired")
+                block_k == 128 else "paired")
     if schedule not in ("paired", "pipelined"):
         raise ValueError(f"unknown schedule {schedule!r}")
     return schedule
@@ -246,8 +247,8 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
     ``schedule``: "paired" (two query heads of a GQA group per CTA, sharing
     each K/V tile), "pipelined" (one query head per CTA, Q.K^T of the next
     tiles issued ahead of the current P.V; Bq = 128, Bk = 128 or 224) or
-    "auto" (``resolve_schedule``: pipelined for gated 128 x 128 calls without
-    mean correction, else paired).  The choice never changes the bitmap or
+    "auto" (``resolve_schedule``: pipelined for gated 128 x 128 calls, else
+    paired).  The choice never changes the bitmap or
     the counts; outputs differ only in floating-point rounding order."""
     if out is None:
         out = torch.empty_like(q)

@@ -277,11 +277,12 @@ static cudaError_t dispatch_t(int d, int nq, Variant v, const Maps& m, const Dev
 }
 
 // The pipelined schedule (bsfa_xs_kernel, BSFA_FLAG_PIPELINED): 128 x 128
-// semantic blocks, no mean correction.
+// semantic blocks (with or without mean correction), or the 128 x 224 tile.
 template <int D, int BK, bool F16>
 static cudaError_t dispatch_xs_d(Variant v, const Maps& m, const DevParams& p, int grid,
                                  cudaStream_t st) {
   if constexpr (BK == 128) {
+    if (v.corr) return launch_xs<D, BK, true, false, F16, false, false, true>(m, p, grid, st);
     if (v.paged) return v.gating ? launch_xs<D, BK, true, false, F16, false, true>(m, p, grid, st)
                                  : launch_xs<D, BK, false, false, F16, false, true>(m, p, grid, st);
   }
@@ -373,10 +374,10 @@ static bsfa_status validate(const bsfa_fwd_params* p) {
   if (p->flags & ~static_cast<unsigned>(BSFA_FLAG_V_ALWAYS | BSFA_FLAG_MEAN_CORRECTION |
                                         BSFA_FLAG_PIPELINED))
     return BSFA_ERR_UNSUPPORTED;
-  // The pipelined schedule: 128 x 128 semantic blocks, no mean correction.
+  // The pipelined schedule: Bq = 128, Bk = 128 or 224 (mean correction with
+  // Bk = 128 only, as in every schedule).
   if ((p->flags & BSFA_FLAG_PIPELINED) &&
-      (p->block_q != TILE || (p->block_k != TILE && p->block_k != 224) ||
-       (p->flags & BSFA_FLAG_MEAN_CORRECTION)))
+      (p->block_q != TILE || (p->block_k != TILE && p->block_k != 224)))
     return BSFA_ERR_UNSUPPORTED;
   // Semantic blocks: Bq, Bk in {64, 128}, or the 128 x 224 tile.
   const bool tile224 = p->block_q == TILE && p->block_k == 224;

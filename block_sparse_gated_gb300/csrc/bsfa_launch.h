@@ -17,9 +17,11 @@ struct Maps {
 template <int D, int NQ, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED, bool CORR>
 cudaError_t launch_fwd(const Maps& m, const DevParams& p, int grid, cudaStream_t stream);
 
-// Launches bsfa_xs_kernel<D, BK, GATING, CALIB, F16, VALL, PAGED> (one query
-// head per CTA, 128-row query tiles, key tiles of BK = 128 or 224).
-template <int D, int BK, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
+// Launches bsfa_xs_kernel<D, BK, GATING, CALIB, F16, VALL, PAGED, CORR> (one
+// query head per CTA, 128-row query tiles, key tiles of BK = 128 or 224; CORR:
+// mean correction, BK = 128).
+template <int D, int BK, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED,
+          bool CORR = false>
 cudaError_t launch_xs(const Maps& m, const DevParams& p, int grid, cudaStream_t stream);
 
 }  // namespace bsfa

@@ -25,7 +25,11 @@
 // each row's maximum against its running max) decides the tile, and a
 // skipped tile gets no V load, no exp and no P.V.  With CALIB the kernel
 // only computes Q.K^T and records sigma * (tile maximum) of every candidate
-// tile (the calibration pass of Key Designs 1).
+// tile (the calibration pass of Key Designs 1).  With CORR (mean correction,
+// "FlashPrefill V2") a unit's key tiles are followed by ceil(I / 128)
+// correction tiles through the same roles: the producer loads key means,
+// the V loader value means, and the softmax runs them in a loop of its own
+// after the key tiles (see the CORR note at the kernel).
 //
 // Roles (384 threads, one CTA per SM, persistent over a heaviest-first list
 // of (KV head, query tile, query head) units):
@@ -61,6 +65,9 @@ struct XsCtrl {
   float xmax[2][2][128]; // per (tile parity, column half, row): half-row maximum
   float xl[2][128];      // per (column half, row): share of the normaliser
   float xw[2][8];        // calibration: per (tile parity, softmax warp) maximum
+  // Mean correction: kept bits of the unit's candidate key blocks (bit j of
+  // word j / 32 = block j kept), written by the bookkeeping warp.
+  uint32_t kbits[CORR_WORDS];
   int abort;
 };
 
@@ -120,11 +127,21 @@ __device__ __forceinline__ void xs_issue_pv(uint32_t d_tmem, uint32_t p_tmem, ui
     umma_ts(d_tmem, p_tmem + kk * 8, dv + ((kk * 2048) >> 4), idesc, (kk > 0 || acc) ? 1u : 0u);
 }
 
-template <int D, int BK, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED>
+// CORR (gated, BK = 128, contiguous K/V): mean correction.  After a unit's key
+// tiles come ceil(I / 128) correction tiles through the same pipeline: their
+// "keys" and "values" are the block means of 128 consecutive key blocks
+// (tmKb, tmVb), and only the candidate blocks this head skipped enter them,
+// with the logit shifted by ln(Bk) so that one mean stands for the block's Bk
+// keys ("FlashPrefill V2", mean correction).
+template <int D, int BK, bool GATING, bool CALIB, bool F16, bool VALL, bool PAGED,
+          bool CORR = false>
 __global__ void __launch_bounds__(384, 1)
     bsfa_xs_kernel(const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const DevParams p) {
+                   const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmKb,
+                   const __grid_constant__ CUtensorMap tmVb, const DevParams p) {
+  static_assert(!CORR || (GATING && !CALIB && !VALL && !PAGED && BK == 128), "mean correction");
   using LY = XsLayout<D, BK, CALIB>;
   constexpr int NB = LY::NB, KST = LY::KST, VST = LY::VST;
   // Q.K^T from a warp of its own (warp 2) when there are several score
@@ -178,6 +195,10 @@ __global__ void __launch_bounds__(384, 1)
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmK);
     if (!CALIB) prefetch_tensormap(&tmV);
+    if (CORR) {
+      prefetch_tensormap(&tmKb);
+      prefetch_tensormap(&tmVb);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&c->tmem_base, LY::NCOLS);
@@ -206,6 +227,7 @@ __global__ void __launch_bounds__(384, 1)
       const int h = kvh * p.group + rem % p.group;
       const int4 si = p.seqinfo[t.x];
       const int n = xs_ntiles<BK>(t.y, si.y);
+      const int ntt = n + (CORR ? (t.y + TILE - 1) / TILE : 0);  // + correction tiles
       if (!(ok = wait_all(&c->q_empty, (uc & 1) ^ 1, abort, p.err, ERR_WAIT_Q_EMPTY))) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(&c->q_full, TQ);
@@ -214,11 +236,13 @@ __global__ void __launch_bounds__(384, 1)
       }
       __syncwarp();
       last_q = static_cast<int>(uc);
-      for (int J = 0; J < n; ++J) {
+      for (int J = 0; J < ntt; ++J) {
         // A K tile's coordinates: the sequence's token base, or (paged, BK =
-        // 128 only) its page from the block table.
+        // 128 only) its page from the block table.  A correction tile reads
+        // the key means of blocks [128 (J - n), +128) of the sequence.
         const int2 cc = PAGED ? kv_tile_coord<PAGED>(p, si, t.x, J)
                               : make_int2(si.x + J * BK, si.w);
+        const bool mean_tile = CORR && J >= n;
         {
           const uint32_t st = kc % KST;
           // With as many K stages as score buffers, Q.K^T number kc reads K
@@ -229,9 +253,14 @@ __global__ void __launch_bounds__(384, 1)
             break;
           if (elect_one()) {
             mbar_arrive_expect_tx(&c->k_full[st], TKV);
-            for (int hf = 0; hf < NHALF; ++hf)
-              tma_load_4d(sK + st * TKV + hf * KHALF, &tmK, &c->k_full[st], hf * 64, cc.x, kvh,
-                          cc.y);
+            for (int hf = 0; hf < NHALF; ++hf) {
+              if (mean_tile)
+                tma_load_4d(sK + st * TKV + hf * KHALF, &tmKb, &c->k_full[st], hf * 64,
+                            si.z + (J - n) * TILE, kvh, 0);
+              else
+                tma_load_4d(sK + st * TKV + hf * KHALF, &tmK, &c->k_full[st], hf * 64, cc.x, kvh,
+                            cc.y);
+            }
           }
           __syncwarp();
           ++kc;
@@ -258,7 +287,8 @@ __global__ void __launch_bounds__(384, 1)
       const int2 t = p.tiles[rem / p.group];
       const int4 si = p.seqinfo[t.x];
       const int n = xs_ntiles<BK>(t.y, si.y);
-      for (int J = 0; J < n; ++J, ++tc) {
+      const int ntt = n + (CORR ? (t.y + TILE - 1) / TILE : 0);
+      for (int J = 0; J < ntt; ++J, ++tc) {
         const int2 cc = PAGED ? kv_tile_coord<PAGED>(p, si, t.x, J)
                               : make_int2(si.x + J * BK, si.w);  // before the waits
         // Also in a unit whose gate keeps everything, V waits for each
@@ -282,9 +312,14 @@ __global__ void __launch_bounds__(384, 1)
           break;
         if (elect_one()) {
           mbar_arrive_expect_tx(&c->v_full[st], TKV);
-          for (int hf = 0; hf < NHALF; ++hf)
-            tma_load_4d(sV + st * TKV + hf * KHALF, &tmV, &c->v_full[st], hf * 64, cc.x, kvh,
-                        cc.y);
+          for (int hf = 0; hf < NHALF; ++hf) {
+            if (CORR && J >= n)  // value means of key blocks [128 (J - n), +128)
+              tma_load_4d(sV + st * TKV + hf * KHALF, &tmVb, &c->v_full[st], hf * 64,
+                          si.z + (J - n) * TILE, kvh, 0);
+            else
+              tma_load_4d(sV + st * TKV + hf * KHALF, &tmV, &c->v_full[st], hf * 64, cc.x, kvh,
+                          cc.y);
+          }
         }
         __syncwarp();
         ++vc;
@@ -340,9 +375,11 @@ __global__ void __launch_bounds__(384, 1)
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
-      const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
-      // A unit whose gate keeps everything: no decision to read (the softmax
-      // still publishes them, so the phases stay one per tile).
+      const int nk = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
+      const int n = nk + (CORR ? (t.y + TILE - 1) / TILE : 0);  // + correction tiles
+      // A unit whose gate keeps everything: no decision to read for its key
+      // tiles (the softmax still publishes them, so the phases stay one per
+      // tile).  Correction tiles are read even then.
       const bool triv = GATING && !CALIB && unit_gate_trivial(p, kvh * p.group + rem % p.group, t.y);
       if constexpr (!SPLIT) {
         if (!(ok = wait_all(&c->q_full, uc & 1, abort, p.err, ERR_WAIT_Q_FULL))) break;
@@ -369,7 +406,7 @@ __global__ void __launch_bounds__(384, 1)
         // saw it so.
         const uint32_t vst = vc % VSTN;
         bool keep = true;
-        if (triv) {
+        if (triv && (!CORR || J < nk)) {
           // keep
         } else if constexpr (GATING && SPLIT) {
           // Q.K^T run ahead of this warp through skipped tiles, so the word
@@ -477,7 +514,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
-      const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
+      const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y) + (CORR ? (t.y + TILE - 1) / TILE : 0);
       if (!(ok = wait_all(&c->q_full, uc & 1, abort, p.err, ERR_WAIT_Q_FULL))) break;
       for (int j = 0; j < n; ++j, ++g) {
         const uint32_t b = g % NB, kst = g % KST;
@@ -768,16 +805,136 @@ __global__ void __launch_bounds__(384, 1)
             ++cnt_diag;
           }
           if (kept) bm_word |= 1u << (J & 31);
-          if (p.bitmap != nullptr && ((J & 31) == 31 || J == n - 1)) {
-            const int4 si = p.seqinfo[p.tiles[(u % per_kv) / p.group].x];
-            if (lane == 0)
-              p.bitmap[((long long)(si.z + I) * p.Hq + h) * (long long)p.words + (J >> 5)] = bm_word;
+          // Mean correction: the kept bits of the candidates, complete before
+          // the diagonal tile's barrier, which every correction tile follows.
+          if (CORR && cand && lane == 0 && ((J & 31) == 31 || J == I - 1))
+            c->kbits[J >> 5] = bm_word;
+          if ((p.bitmap != nullptr || CORR) && ((J & 31) == 31 || J == n - 1)) {
+            if (p.bitmap != nullptr) {
+              const int4 si = p.seqinfo[p.tiles[(u % per_kv) / p.group].x];
+              if (lane == 0)
+                p.bitmap[((long long)(si.z + I) * p.Hq + h) * (long long)p.words + (J >> 5)] =
+                    bm_word;
+            }
             bm_word = 0;
           }
         }
       }
       if (!ok) break;
       if constexpr (CALIB) continue;
+
+      if constexpr (CORR) {
+        // ---- correction tiles, a loop of their own so that the key tiles'
+        // loop stays as without the option.  Tile ci holds the means of key
+        // blocks [128 ci, 128 ci + 128); my 64 entries are blocks kb0 ..
+        // kb0 + 63.  An entry enters when its block is a candidate (block <
+        // I) that this head skipped (the kept bits are complete: the diagonal
+        // tile's barrier came after the last of them), with ln(Bk) added to
+        // its logit (corr_shift, raw score units).  The tile is kept when
+        // some entry enters; then the same vote barrier, exchange, rescale and
+        // P hand-off as a key tile.
+        const int nct = (I + TILE - 1) / TILE;
+        for (int ci = 0; ci < nct; ++ci, ++tc) {
+          const uint32_t b = tc % NB;
+          const bool okl = wait_bar(&c->s_full[b], (tc / NB) & 1, abort, p.err, ERR_WAIT_S_FULL);
+          __syncwarp();
+          tc_fence_after();
+          const int kb0 = ci * TILE + ch * HK;
+          const uint32_t tS = tmem + tlane + b * 128 + ch * HK;
+          uint32_t sr[2][32], inc[2];
+          tmem_ld32(tS, sr[0]);
+          tmem_ld32(tS + 32, sr[1]);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int lim = I - kb0 - 32 * q;
+            const uint32_t cm = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
+            inc[q] = lim > 0 ? cm & ~c->kbits[(kb0 >> 5) + q] : 0u;
+          }
+          tmem_wait_ld();
+          float lm = -CUDART_INF_F;
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if ((inc[q] >> e) & 1u) lm = fmaxf(lm, __uint_as_float(sr[q][e]));
+          if (lm != -CUDART_INF_F) lm += p.corr_shift;
+          const bool need_x = rvalid && (lm - m_used) * sc > RESCALE_LOG2;
+          tc_fence_before();
+          const bool wx = __any_sync(0xffffffffu, !okl || need_x);
+          const bool wv = (inc[0] | inc[1]) != 0u;  // the same in every row of my half
+          const uint32_t nv = bar_red_popc(bar_id, NBAR, lane == 0 ? wx : (lane <= 16 && wv));
+          const bool kept = nv >= 16u;
+          float rowmax = lm;
+          const bool exact = (nv & 15u) != 0u;
+          if (exact) {
+            c->xmax[tc & 1][ch][row] = lm;
+            ok = bar_red_and(bar_id, NBAR, okl);
+            if (!ok) break;
+            rowmax = fmaxf(lm, c->xmax[tc & 1][ch ^ 1][row]);
+          }
+          if (lead_warp) {
+            st_release_u32(&c->dec[b], ((tc & DEC_STAMP_MASK) << DEC_BITS) | (kept ? 1u : 0u));
+            mbar_arrive(&c->dec_full[b]);
+            if (!kept && elect_one()) mbar_arrive(&c->buf_free[b]);
+            __syncwarp();
+          }
+          if (kept) {
+            if (exact) {
+              const float m_new = fmaxf(m_used, rowmax);
+              const bool resc = (m_new - m_used) * sc > RESCALE_LOG2;
+              float alpha = 1.f;
+              if (resc) {
+                alpha = ex2_approx((m_used - m_new) * sc);
+                m_used = m_new;
+                l *= alpha;
+              }
+              if (o_init && __any_sync(0xffffffffu, resc)) {
+                wait_bar(&c->pv_done[(kn - 1) & 1], ((kn - 1) >> 1) & 1, abort, p.err,
+                         ERR_WAIT_O_FULL);
+                __syncwarp();
+                tc_fence_after();
+#pragma unroll 1
+                for (int q = 0; q < DH / 16; ++q) {
+                  uint32_t orr[16];
+                  tmem_ld16(tO + q * 16, orr);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int e = 0; e < 16; ++e)
+                    orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                  tmem_st16(tO + q * 16, orr);
+                }
+              }
+            }
+            const uint32_t tP = tmem + tlane + b * 128 + ch * (HK / 2);
+            const float bias =
+                p.corr_shift * sc - ((m_used == -CUDART_INF_F) ? 0.f : m_used * sc);
+            float lsum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float x0 = __uint_as_float(sr[q][2 * e]);
+                const float x1 = __uint_as_float(sr[q][2 * e + 1]);
+                const float p0 =
+                    ((inc[q] >> (2 * e)) & 1u) ? ex2_approx(fmaf(x0, sc, bias)) : 0.f;
+                const float p1 =
+                    ((inc[q] >> (2 * e + 1)) & 1u) ? ex2_approx(fmaf(x1, sc, bias)) : 0.f;
+                lsum += p0 + p1;
+                pk[e] = pack_x2<F16>(p0, p1);
+              }
+              tmem_st16(tP + q * 16, pk);
+            }
+            l += lsum;
+            tmem_wait_st();
+            o_init = true;
+            ++kn;
+          }
+          tc_fence_before();
+          mbar_arrive(ch == 0 ? &c->ph_full[b] : &c->p_full[b]);
+        }
+        if (!ok) break;
+      }
 
       // ---- epilogue: O / l -> 16-bit, log-sum-exp, bitmap tail
       const int4 si = p.seqinfo[p.tiles[(u % per_kv) / p.group].x];

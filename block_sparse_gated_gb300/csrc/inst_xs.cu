@@ -28,5 +28,14 @@ BSFA_XS(64, true, true, false, true)
 BSFA_XS(64, false, false, false, true)
 BSFA_XS(64, false, true, false, true)
 #undef BSFA_XS
+// Mean correction (gated, contiguous K/V).
+template cudaError_t launch_xs<128, 128, true, false, false, false, false, true>(
+    const Maps&, const DevParams&, int, cudaStream_t);
+template cudaError_t launch_xs<128, 128, true, false, true, false, false, true>(
+    const Maps&, const DevParams&, int, cudaStream_t);
+template cudaError_t launch_xs<64, 128, true, false, false, false, false, true>(
+    const Maps&, const DevParams&, int, cudaStream_t);
+template cudaError_t launch_xs<64, 128, true, false, true, false, false, true>(
+    const Maps&, const DevParams&, int, cudaStream_t);
 
 }  // namespace bsfa

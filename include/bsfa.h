@@ -114,17 +114,17 @@ typedef enum {
    * of the normaliser).  Paired (flags = 0): a CTA holds two query heads of
    * one GQA group that share every K/V tile, with one score buffer each; a
    * head's next Q.K^T waits for its current P.V.  Pipelined: a CTA holds one
-   * query head with two score buffers, so the Q.K^T of tile t + 2 is issued
-   * as soon as tile t's decision (a skip) or P (a keep) is in, ahead of its
-   * P.V ("Skipping attention blocks was the easy part", section "Cross-stage
-   * P").  Requires block_q == 128, block_k == 128 or 224, and no mean
-   * correction, else BSFA_ERR_UNSUPPORTED.  With three score buffers and the
-   * Q.K^T issued by a warp of its own, it is the faster schedule for gated
-   * calls (threshold or lambda) with 128 x 128 blocks once tiles are
-   * skipped (the Python binding's default picks it there); the paired
-   * schedule is faster with the gate compiled out.  The 128 x 224 tile
-   * always runs one query head per CTA (its 224-column score buffer fits
-   * TMEM once, not twice), with or without this flag. */
+   * query head with three score buffers, and a warp of its own issues the
+   * Q.K^T of tile t + 3 as soon as tile t is done with its buffer (skipped,
+   * or its P.V complete), ahead of the P.V in flight ("Skipping attention
+   * blocks was the easy part", section "Cross-stage P").  Requires
+   * block_q == 128 and block_k == 128 or 224, else BSFA_ERR_UNSUPPORTED;
+   * mean correction runs in both schedules (block_k == 128).  It is the
+   * faster schedule for gated calls (threshold or lambda) with 128 x 128
+   * blocks once tiles are skipped (the Python binding's default picks it
+   * there); the paired schedule is faster with the gate compiled out.  The
+   * 128 x 224 tile always runs one query head per CTA (its 224-column score
+   * buffer fits TMEM once, not twice), with or without this flag. */
   BSFA_FLAG_PIPELINED = 4
 } bsfa_flag;
 

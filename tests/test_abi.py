@@ -73,7 +73,7 @@ def test_host_side_validation_without_gpu(libpath):
     p.flags, p.block_k = _native.FLAG_PIPELINED, 64
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # pipelined: 128 x 128 blocks only
     p.flags, p.block_k = _native.FLAG_PIPELINED | _native.FLAG_MEAN_CORRECTION, 128
-    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # pipelined: no mean correction
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # accepted up to the null tensors
     p.flags = _native.FLAG_PIPELINED
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 1  # accepted up to the null tensors
     # The 128 x 224 tile: accepted with 128-row query blocks only, contiguous

@@ -1,7 +1,9 @@
 """Mean correction for skipped blocks (the stand-in of the "FlashPrefill V2"
 summary, agihunt.info) on the GPU path, against the fp64 oracle with the same
 option.  The gate's decisions do not depend on it, so the bitmaps are still
-compared bit for bit; outputs and log-sum-exp use the bf16 tolerances."""
+compared bit for bit; outputs and log-sum-exp use the bf16 tolerances.  Both
+kernels run it: the paired kernel and the one-head (pipelined) kernel, each
+with its own correction tiles."""
 import math
 
 import numpy as np
@@ -15,6 +17,7 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 B = 128
+SCHEDULES = ["paired", "pipelined"]
 
 
 def _bsfa():
@@ -30,8 +33,9 @@ def _run(q, k, v, **kw):
     return r
 
 
+@pytest.mark.parametrize("schedule", SCHEDULES)
 @pytest.mark.parametrize("Hq,Hkv,L,d", [(4, 2, 1000, 128), (2, 1, 777, 64), (1, 1, 640, 128)])
-def test_corrected_threshold_gate_matches_oracle(cuda_device, Hq, Hkv, L, d):
+def test_corrected_threshold_gate_matches_oracle(cuda_device, Hq, Hkv, L, d, schedule):
     x = wl.layer_inputs(Hq, Hkv, L, d, 400 + L, skip_rate=0.4)
     q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
     sigma = gu.default_sigma(d)
@@ -39,7 +43,7 @@ def test_corrected_threshold_gate_matches_oracle(cuda_device, Hq, Hkv, L, d):
     T, _, _ = gu.guarded_thresholds(q64, k64, T, B, B, sigma)
     r = _run(x.q.to(cuda_device)[None], x.k.to(cuda_device)[None], x.v.to(cuda_device)[None],
              mode="threshold", thresholds=torch.from_numpy(T).to(cuda_device),
-             mean_correction=True)
+             mean_correction=True, schedule=schedule)
     ref = orc.prefill(q64, k64, v64, Bq=B, Bk=B, thresholds=T.astype(np.float64),
                       mean_correction=True)
     bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, [L], B, B)
@@ -50,7 +54,8 @@ def test_corrected_threshold_gate_matches_oracle(cuda_device, Hq, Hkv, L, d):
                     mean_abs=gu.LSE_ABS)
 
 
-def test_corrected_lambda_gate_varlen_matches_oracle(cuda_device):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_corrected_lambda_gate_varlen_matches_oracle(cuda_device, schedule):
     Hq, Hkv, d = 4, 2, 128
     lens = [300, 1000, 129, 0, 513]
     parts = [wl.layer_inputs(Hq, Hkv, Ln, d, 420 + n, skip_rate=0.5) if Ln else None
@@ -66,7 +71,7 @@ def test_corrected_lambda_gate_varlen_matches_oracle(cuda_device):
     r = _bsfa().prefill(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
                         cu_seqlens=cu.to(cuda_device), max_seqlen=max(lens), mode="lambda",
                         log_lambda=ll, mean_correction=True, return_bitmap=True,
-                        return_lse=True)
+                        return_lse=True, schedule=schedule)
     torch.cuda.synchronize()
     assert _bsfa().api.device_error() == 0
     ref = orc.prefill_varlen(gu.to64(q), gu.to64(k), gu.to64(v), cu.numpy(), Bq=B, Bk=B,
@@ -80,7 +85,8 @@ def test_corrected_lambda_gate_varlen_matches_oracle(cuda_device):
     gu.assert_close(gu.to64(r["lse"]), ref["lse"], "lse", max_abs=gu.LSE_ABS, mean_abs=gu.LSE_ABS)
 
 
-def test_constant_blocks_make_the_correction_exact(cuda_device):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_constant_blocks_make_the_correction_exact(cuda_device, schedule):
     """K and V constant inside every 128-key block: with every candidate
     skipped (T = +inf), the corrected output equals dense attention."""
     Hq, Hkv, L, d = 2, 1, 900, 128
@@ -93,7 +99,8 @@ def test_constant_blocks_make_the_correction_exact(cuda_device):
     q = torch.randn(Hq, L, d, generator=g).to(torch.bfloat16)
     qd, kd, vd = (t.to(cuda_device)[None] for t in (q, k, v))
     T = torch.full((Hq, 1), math.inf, device=cuda_device)
-    corr = _run(qd, kd, vd, mode="threshold", thresholds=T, mean_correction=True)
+    corr = _run(qd, kd, vd, mode="threshold", thresholds=T, mean_correction=True,
+                schedule=schedule)
     dense = _run(qd, kd, vd, mode="none")
     plain = _run(qd, kd, vd, mode="threshold", thresholds=T)
     assert int(corr["counts"][0]) == 0  # every candidate skipped
@@ -102,30 +109,69 @@ def test_constant_blocks_make_the_correction_exact(cuda_device):
     assert err_plain > 0.05  # without the stand-ins the outputs differ
 
 
-def test_correction_without_skips_changes_nothing(cuda_device):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_correction_without_skips_changes_nothing(cuda_device, schedule):
+    """Nothing skipped: every correction tile is skipped too, and the output
+    is the same bytes as without the option, in the same kernel."""
     Hq, Hkv, L, d = 4, 2, 700, 128
     x = wl.layer_inputs(Hq, Hkv, L, d, 440)
     q, k, v = (t.to(cuda_device)[None] for t in (x.q, x.k, x.v))
     T = torch.full((Hq, 1), -math.inf, device=cuda_device)
-    # Mean correction runs in the paired kernel: compare within it.
-    a = _run(q, k, v, mode="threshold", thresholds=T, schedule="paired")
-    b = _run(q, k, v, mode="threshold", thresholds=T, mean_correction=True)
+    a = _run(q, k, v, mode="threshold", thresholds=T, schedule=schedule)
+    b = _run(q, k, v, mode="threshold", thresholds=T, mean_correction=True, schedule=schedule)
     for key in ("out", "lse", "bitmap", "counts"):
         assert torch.equal(a[key], b[key]), key
 
 
-def test_fp16_corrected_matches_oracle(cuda_device):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_fp16_corrected_matches_oracle(cuda_device, schedule):
     Hq, Hkv, L, d = 2, 2, 600, 64
     x = wl.layer_inputs(Hq, Hkv, L, d, 450, skip_rate=0.5, dtype=torch.float16)
     q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
     ll = gu.guarded_log_lambda(-1.0, B, B, gu.default_sigma(d), [(q64, k64)])
     r = _run(x.q.to(cuda_device)[None], x.k.to(cuda_device)[None], x.v.to(cuda_device)[None],
-             mode="lambda", log_lambda=ll, mean_correction=True)
+             mode="lambda", log_lambda=ll, mean_correction=True, schedule=schedule)
     ref = orc.prefill(q64, k64, v64, Bq=B, Bk=B, mode="lambda", log_lambda=ll,
                       mean_correction=True)
     bits, _ = gu.unpack_bitmap(r["bitmap"], Hq, [L], B, B)
     assert np.array_equal(bits[0], ref["keep"])
     gu.assert_close(gu.to64(r["out"][0]), ref["out"], "out", max_abs=4e-3, mean_abs=4e-4)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_correction_spans_several_mean_tiles(cuda_device, schedule):
+    """A 16.9K-token layer: query blocks past 128 candidates take two
+    correction tiles, and the kept bits of a row fill several 32-block words.
+    About 70% of each compared row's candidates are skipped; the oracle
+    evaluates the sampled query blocks of both heads (the GPU computes all)."""
+    Hq, Hkv, d = 2, 1, 128
+    L = 131 * B + 77
+    x = wl.layer_inputs(Hq, Hkv, L, d, 470, skip_rate=0.5)
+    q64, k64, v64 = gu.to64(x.q), gu.to64(x.k), gu.to64(x.v)
+    sigma = gu.default_sigma(d)
+    nq = orc.num_blocks(L, B)
+    sampled = [0, 1, 31, 32, 33, 64, 100, 127, 128, 129, nq - 1]
+    blocks = [(h, i) for h in range(Hq) for i in sampled]
+    rng = np.random.default_rng(470)
+    T = np.zeros((Hq, nq), dtype=np.float32)  # rows not compared: any table entry
+    for h, i in blocks:
+        m = orc.candidate_maxima(q64[h], k64[h // (Hq // Hkv)], i, B, B, sigma)
+        T[h, i] = np.quantile(m, 0.7) + 0.05 * rng.standard_normal() if m else -np.inf
+    T, _, _ = gu.guarded_thresholds(q64, k64, T, B, B, sigma, blocks=blocks)
+    r = _run(x.q.to(cuda_device)[None], x.k.to(cuda_device)[None], x.v.to(cuda_device)[None],
+             mode="threshold", thresholds=torch.from_numpy(T).to(cuda_device),
+             mean_correction=True, schedule=schedule)
+    ref = orc.prefill(q64, k64, v64, Bq=B, Bk=B, thresholds=T.astype(np.float64),
+                      blocks=blocks, mean_correction=True)
+    bits, clean = gu.unpack_bitmap(r["bitmap"], Hq, [L], B, B)
+    assert clean
+    for h, i in blocks:
+        assert np.array_equal(bits[0][h, i], ref["keep"][h, i]), (h, i)
+    skipped = sum(int((~ref["keep"][h, i] & ref["candidate"][h, i]).sum()) for h, i in blocks)
+    assert skipped > 800
+    gu.assert_close(gu.to64(r["out"][0]), ref["out"], "out")
+    gu.assert_close(gu.to64(r["lse"]).reshape(Hq, L), ref["lse"], "lse", max_abs=gu.LSE_ABS,
+                    mean_abs=gu.LSE_ABS)
 
 
 def test_block_mean_pass_head_limit(cuda_device):

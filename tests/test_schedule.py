@@ -1,6 +1,7 @@
 """The binding's schedule choice (host logic, no GPU): "auto" takes the
-one-head kernel for gated 128 x 128 calls without mean correction and the
-paired kernel otherwise; the 128 x 224 tile has only the one-head kernel."""
+one-head kernel for gated 128 x 128 calls (with or without mean correction)
+and the paired kernel otherwise; the 128 x 224 tile has only the one-head
+kernel."""
 import pytest
 
 from block_sparse_gated_gb300.api import resolve_schedule
@@ -9,10 +10,11 @@ from block_sparse_gated_gb300.api import resolve_schedule
 @pytest.mark.parametrize("mode", ["threshold", "lambda"])
 def test_auto_takes_pipelined_for_gated_128(mode):
     assert resolve_schedule("auto", mode=mode) == "pipelined"
+    assert resolve_schedule("auto", mode=mode, mean_correction=True) == "pipelined"
 
 
 @pytest.mark.parametrize("kw", [dict(mode="none"), dict(block_q=64), dict(block_k=64),
-                                dict(block_q=64, block_k=64), dict(mean_correction=True)])
+                                dict(block_q=64, block_k=64)])
 def test_auto_takes_paired_elsewhere(kw):
     args = dict(mode="threshold")
     args.update(kw)

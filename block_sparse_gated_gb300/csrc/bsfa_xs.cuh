@@ -97,6 +97,19 @@ struct XsLayout {
   static_assert(KST <= 4 && VST <= 2 && NB <= 3, "ring sizes of XsCtrl");
 };
 
+// The CTA's k-th unit.  Waves of gridDim.x units alternate direction over the
+// CTAs (boustrophedon): the CTA that takes a wave's heaviest unit takes the
+// next wave's lightest, so the CTAs' cumulative work stays level and the
+// units of a wave stream a KV head's K/V prefix together, close enough in
+// time for each tile to be fetched into L2 once.  (Dealt round-robin, the
+// first CTAs would take the heaviest unit of every wave and drift a whole
+// unit ahead of the last ones within a KV head.)  Increasing in k for a
+// given CTA, so a loop may stop at the first unit past the end.
+__device__ __forceinline__ int xs_unit(int k) {
+  const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  return k * g + ((k & 1) ? g - 1 - b : b);
+}
+
 // Key tiles visible to query tile I of a length-len sequence: those starting
 // at or before the tile's last row.
 template <int BK>
@@ -221,7 +234,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t kc = 0, uc = 0;
     int last_q = -1;  // index of the last unit whose Q load was issued
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k), ++uc) {
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int h = kvh * p.group + rem % p.group;
@@ -282,7 +295,7 @@ __global__ void __launch_bounds__(384, 1)
     // is free).  A warp of its own, so that K loads never queue behind V.
     uint32_t vc = 0, tc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k)) {
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int4 si = p.seqinfo[t.x];
@@ -372,7 +385,7 @@ __global__ void __launch_bounds__(384, 1)
       ++kc;
       return true;
     };
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k), ++uc) {
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int nk = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
@@ -511,7 +524,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
     uint32_t g = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k), ++uc) {
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y) + (CORR ? (t.y + TILE - 1) / TILE : 0);
@@ -572,7 +585,7 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     uint32_t cnt_kept = 0, cnt_cand = 0, cnt_diag = 0;
 
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++uc) {
+    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k), ++uc) {
       int I, len, h;
       {
         const int kvh = u / per_kv, rem = u - kvh * per_kv;

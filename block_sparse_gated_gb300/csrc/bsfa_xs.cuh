@@ -97,18 +97,41 @@ struct XsLayout {
   static_assert(KST <= 4 && VST <= 2 && NB <= 3, "ring sizes of XsCtrl");
 };
 
-// The CTA's k-th unit.  Waves of gridDim.x units alternate direction over the
-// CTAs (boustrophedon): the CTA that takes a wave's heaviest unit takes the
-// next wave's lightest, so the CTAs' cumulative work stays level and the
-// units of a wave stream a KV head's K/V prefix together, close enough in
-// time for each tile to be fetched into L2 once.  (Dealt round-robin, the
-// first CTAs would take the heaviest unit of every wave and drift a whole
-// unit ahead of the last ones within a KV head.)  Increasing in k for a
-// given CTA, so a loop may stop at the first unit past the end.
-__device__ __forceinline__ int xs_unit(int k) {
-  const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
-  return k * g + ((k & 1) ? g - 1 - b : b);
-}
+// The CTA's units, in order.  Each KV head's units (heaviest first) are dealt
+// in waves of gridDim.x, and the waves alternate direction over the CTAs
+// (boustrophedon): the CTA that takes a wave's heaviest unit takes the next
+// wave's lightest, so the CTAs' cumulative work stays level and the units of
+// a wave stream the KV head's K/V prefix together, close enough in time for
+// each tile to be fetched into L2 once.  The first wave's direction flips
+// from one KV head to the next, which also levels the partial last waves.
+// (Dealt round-robin, the first CTAs took the heaviest unit of every wave
+// and drifted a whole unit ahead of the last ones within a KV head.)  Every
+// role of the CTA walks the same sequence.
+struct XsUnits {
+  int per_kv, hkv, h, w, u;  // u: the current unit, -1 past the end
+  __device__ __forceinline__ XsUnits(int per_kv_, int hkv_)
+      : per_kv(per_kv_), hkv(hkv_), h(0), w(-1), u(-1) {
+    next();
+  }
+  __device__ __forceinline__ bool valid() const { return u >= 0; }
+  __device__ __forceinline__ void next() {
+    const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    for (;;) {
+      if (++w * g >= per_kv) {  // past this KV head's last wave
+        w = 0;
+        if (++h >= hkv) {
+          u = -1;
+          return;
+        }
+      }
+      const int ul = w * g + (((w + h) & 1) ? g - 1 - b : b);
+      if (ul < per_kv) {
+        u = h * per_kv + ul;
+        return;
+      }
+    }
+  }
+};
 
 // Key tiles visible to query tile I of a length-len sequence: those starting
 // at or before the tile's last row.
@@ -227,14 +250,14 @@ __global__ void __launch_bounds__(384, 1)
   // together, out of L2).
   const int ntot = *p.ntiles_total;
   const int per_kv = ntot * p.group;
-  const int total_units = per_kv * p.Hkv;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t kc = 0, uc = 0;
     int last_q = -1;  // index of the last unit whose Q load was issued
     bool ok = true;
-    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k), ++uc) {
+    for (XsUnits it(per_kv, p.Hkv); ok && it.valid(); it.next(), ++uc) {
+      const int u = it.u;
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int h = kvh * p.group + rem % p.group;
@@ -295,7 +318,8 @@ __global__ void __launch_bounds__(384, 1)
     // is free).  A warp of its own, so that K loads never queue behind V.
     uint32_t vc = 0, tc = 0;
     bool ok = true;
-    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k)) {
+    for (XsUnits it(per_kv, p.Hkv); ok && it.valid(); it.next()) {
+      const int u = it.u;
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int4 si = p.seqinfo[t.x];
@@ -385,7 +409,8 @@ __global__ void __launch_bounds__(384, 1)
       ++kc;
       return true;
     };
-    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k), ++uc) {
+    for (XsUnits it(per_kv, p.Hkv); ok && it.valid(); it.next(), ++uc) {
+      const int u = it.u;
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int nk = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y);
@@ -524,7 +549,8 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
     uint32_t g = 0, uc = 0;
     bool ok = true;
-    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k), ++uc) {
+    for (XsUnits it(per_kv, p.Hkv); ok && it.valid(); it.next(), ++uc) {
+      const int u = it.u;
       const int kvh = u / per_kv, rem = u - kvh * per_kv;
       const int2 t = p.tiles[rem / p.group];
       const int n = xs_ntiles<BK>(t.y, p.seqinfo[t.x].y) + (CORR ? (t.y + TILE - 1) / TILE : 0);
@@ -585,7 +611,8 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     uint32_t cnt_kept = 0, cnt_cand = 0, cnt_diag = 0;
 
-    for (int k = 0, u = xs_unit(0); ok && u < total_units; u = xs_unit(++k), ++uc) {
+    for (XsUnits it(per_kv, p.Hkv); ok && it.valid(); it.next(), ++uc) {
+      const int u = it.u;
       int I, len, h;
       {
         const int kvh = u / per_kv, rem = u - kvh * per_kv;

@@ -122,9 +122,10 @@ typedef enum {
    * mean correction runs in both schedules (block_k == 128).  It is the
    * faster schedule for gated calls (threshold or lambda) with 128 x 128
    * blocks once tiles are skipped (the Python binding's default picks it
-   * there); the paired schedule is faster with the gate compiled out.  The
-   * 128 x 224 tile always runs one query head per CTA (its 224-column score
-   * buffer fits TMEM once, not twice), with or without this flag. */
+   * there); with the gate compiled out the two are within a few percent of
+   * each other.  The 128 x 224 tile always runs one query head per CTA (its
+   * 224-column score buffer fits TMEM once, not twice), with or without this
+   * flag. */
   BSFA_FLAG_PIPELINED = 4
 } bsfa_flag;
 

@@ -248,8 +248,8 @@ def prefill(q, k, v, *, block_q=128, block_k=128, softmax_scale=None, mode="thre
     each K/V tile), "pipelined" (one query head per CTA, Q.K^T of the next
     tiles issued ahead of the current P.V; Bq = 128, Bk = 128 or 224) or
     "auto" (``resolve_schedule``: pipelined for gated 128 x 128 calls, else
-    paired).  The choice never changes the bitmap or
-    the counts; outputs differ only in floating-point rounding order."""
+    paired).  The choice never changes the bitmap or the counts; outputs
+    differ only in floating-point rounding order."""
     if out is None:
         out = torch.empty_like(q)
     dev = q.device

@@ -170,8 +170,14 @@ def test_mean_correction_parameters_are_validated_on_the_host(libpath):
     plain = L.bsfa_prefill_workspace_size(ctypes.byref(p))
     p.flags = _native.FLAG_MEAN_CORRECTION
     # the workspace grows by two block-mean tables: 2 KV heads x 8 blocks x 128 x 2 bytes each
-    assert L.bsfa_prefill_workspace_size(ctypes.byref(p)) >= plain + 2 * 2 * 8 * 128 * 2
+    corr = L.bsfa_prefill_workspace_size(ctypes.byref(p))
+    assert corr >= plain + 2 * 2 * 8 * 128 * 2
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 5  # fine up to the missing workspace
+    # Both schedules carry the option, with the same workspace.
+    p.flags = _native.FLAG_MEAN_CORRECTION | _native.FLAG_PIPELINED
+    assert L.bsfa_prefill_workspace_size(ctypes.byref(p)) == corr
+    assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 5
+    p.flags = _native.FLAG_MEAN_CORRECTION
     p.mode = 2
     assert L.bsfa_prefill_fwd(ctypes.byref(p), None) == 2  # nothing is skipped without a gate
     p.mode, p.block_k = 0, 64
